@@ -1,0 +1,167 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA decode library
+ *                 (libmla_decode.so).
+ *
+ * What it computes
+ * ----------------
+ * Multi-head Latent Attention decode in the weight-absorbed form without
+ * materialised absorbed weights.  Source: vLLM PR #14770 "[Attention] MLA get
+ * rid of materialization", PR description.  Instead of precomputing W_Q_UK and
+ * W_UV_O, the decode step runs as sequential bf16 matmuls:
+ *
+ *   1. q-absorb bmm: q_lat[b,t,h] = [ q_nope[b,t,h] . W_UK[h] (512) || q_pe (64) ]
+ *   2. latent attention: every head attends MQA-style to the shared latent
+ *      cache row c_j = [c_kv (512) || k_pe (64)].  Query t of a T-token block
+ *      sees keys [0, L_b - T + t]:
+ *        s_j = scale * (q_lat . c_j),   lse = ln sum_j exp(s_j),
+ *        o_lat = sum_j exp(s_j - lse) * c_j[0:512]
+ *   3. UV bmm: out[b,t,h] = o_lat . W_UV[h] (128)
+ *
+ * The latent cache is paged with 64-token blocks and stored in BF16
+ * ("DeepSeek publica FlashMLA como codigo abierto", feature list: BF16, paged
+ * KV cache with block size 64, optimised for variable-length sequences).
+ * Split-KV over key ranges and the log-sum-exp merge of the partial results
+ * follow the FlashAttention line of work that the same page names as
+ * FlashMLA's inspiration.
+ *
+ * Fixed model dimensions (DeepSeek MLA): qk_nope = 128, qk_rope = 64,
+ * kv_lora = 512, v_head = 128, page_size = 64.  Other values are rejected with
+ * MLA_DECODE_UNSUPPORTED.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - Pointers are DEVICE pointers owned by the caller (for example PyTorch
+ *   tensors), contiguous, 16-byte aligned.  The library keeps no pointer after
+ *   a call returns and allocates no device memory: all scratch lives in the
+ *   caller's workspace (size from mla_decode_workspace_size).
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   All work is enqueued on it; calls do not synchronise the host, except
+ *   mla_decode_check.
+ * - Return value: an mla_decode_status.  Codes 1..4 are detected on the host
+ *   before anything is enqueued (nothing runs).  Codes 5..6 are detected by the
+ *   kernels, written to the workspace status word and reported by
+ *   mla_decode_check; the offending unit of work is skipped or computed on a
+ *   substitute page, never trapped.
+ * - Thread safety: concurrent calls are safe when each uses its own
+ *   workspace.  A plan written into a workspace stays valid for every run with
+ *   the same dims and seq_lens contents (one plan serves all layers of a
+ *   decode step).
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+  int32_t batch;             /* B >= 1: sequences in the decode batch            */
+  int32_t q_len;             /* T in {1, 2}: new query tokens per sequence        */
+  int32_t num_heads;         /* H, multiple of 16, 16 <= H <= 128                 */
+  int32_t qk_nope;           /* must be 128                                       */
+  int32_t qk_rope;           /* must be 64                                        */
+  int32_t kv_lora;           /* must be 512                                       */
+  int32_t v_head;            /* must be 128                                       */
+  int32_t page_size;         /* must be 64                                        */
+  int32_t num_pages;         /* pages in the cache pool (>= 1)                    */
+  int32_t max_pages_per_seq; /* row length of block_table (>= 1)                  */
+} mla_decode_dims;
+
+typedef enum {
+  MLA_DECODE_OK = 0,
+  MLA_DECODE_INVALID_ARG = 1,       /* null / misaligned pointer, bad dims         */
+  MLA_DECODE_UNSUPPORTED = 2,       /* q_len or model dims outside the fixed set   */
+  MLA_DECODE_WORKSPACE_TOO_SMALL = 3,
+  MLA_DECODE_CUDA_ERROR = 4,        /* a CUDA runtime/driver call failed            */
+  MLA_DECODE_DEVICE_BOUNDS = 5,     /* block_table entry outside [0, num_pages) or
+                                       seq_len outside [q_len, max_pages_per_seq*64] */
+  MLA_DECODE_TIMEOUT = 6            /* a bounded device-side wait gave up           */
+} mla_decode_status;
+
+/* Bytes of device workspace needed for `dims` on the current device, with the
+ * default number of work ranges (one per resident decode CTA group).
+ * Needs a CUDA device (queries its SM count); returns CUDA_ERROR without one. */
+int mla_decode_workspace_size(const mla_decode_dims* dims, size_t* bytes);
+
+/* Same, for a plan built with `num_ranges` work ranges (0 = default).  More
+ * ranges means more key splits per sequence; used to exercise the split and
+ * combine paths.  1 <= num_ranges <= 65536. */
+int mla_decode_workspace_size_ex(const mla_decode_dims* dims, int32_t num_ranges,
+                                 size_t* bytes);
+
+/* Step a1, the planner.  Reads seq_lens (device int32 [B]) on the device and
+ * writes into the workspace: the partition of all (sequence, page) work into
+ * equal-cost contiguous ranges, each sequence's split count and its slots for
+ * partial results.  Also clears the workspace status word.  No host sync. */
+int mla_decode_plan(const mla_decode_dims* dims, const int32_t* seq_lens,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* mla_decode_plan with an explicit number of work ranges (0 = default). */
+int mla_decode_plan_ex(const mla_decode_dims* dims, const int32_t* seq_lens,
+                       int32_t num_ranges, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/* Steps a2..a5 for one layer, after mla_decode_plan on the same workspace:
+ *   q           bf16 [B, T, H, 192]   = [q_nope 128 || q_pe 64], RoPE applied
+ *   kv_cache    bf16 [num_pages, 64, 576] = [c_kv 512 || k_pe 64] per token;
+ *               rows past a sequence's length in its last page must be finite
+ *   block_table int32 [B, max_pages_per_seq]: logical page -> physical page;
+ *               entries past ceil(L_b/64) are never read
+ *   seq_lens    int32 [B]: tokens in each sequence INCLUDING its T new tokens
+ *   w_uk        bf16 [H, 128, 512];  w_uv bf16 [H, 512, 128]
+ *   softmax_scale: multiplies q_lat . c_j (e.g. 1/sqrt(192))
+ *   out         bf16 [B, T, H, 128] (written)
+ *   lse         fp32 [B, T, H] (written): natural-log log-sum-exp of the
+ *               scaled scores of each query row
+ * Enqueues four kernels: absorb, attend, combine, up-project. */
+int mla_decode_run(const mla_decode_dims* dims, const void* q, const void* kv_cache,
+                   const int32_t* block_table, const int32_t* seq_lens, const void* w_uk,
+                   const void* w_uv, float softmax_scale, void* out, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* The four steps of mla_decode_run as separate calls, in this order, on one
+ * workspace after mla_decode_plan (for profiling one step at a time).
+ *   absorb:     q, w_uk            -> q_lat (bf16 hi and lo parts, workspace)
+ *   attend:     q_lat, cache, ...  -> o_lat + lse for unsplit sequences,
+ *                                     fp32 partials for split ones
+ *   combine:    partials           -> o_lat + lse for split sequences
+ *   up_project: o_lat, w_uv        -> out                                   */
+int mla_decode_absorb(const mla_decode_dims* dims, const void* q, const void* w_uk,
+                      void* workspace, size_t workspace_bytes, void* stream);
+int mla_decode_attend(const mla_decode_dims* dims, const void* kv_cache,
+                      const int32_t* block_table, const int32_t* seq_lens,
+                      float softmax_scale, float* lse, void* workspace,
+                      size_t workspace_bytes, void* stream);
+int mla_decode_combine(const mla_decode_dims* dims, float softmax_scale, float* lse,
+                       void* workspace, size_t workspace_bytes, void* stream);
+int mla_decode_up_project(const mla_decode_dims* dims, const void* w_uv, void* out,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Waits for `stream`, then returns the first device-side status recorded in
+ * the workspace since the last plan (OK, DEVICE_BOUNDS or TIMEOUT), or
+ * CUDA_ERROR if the stream reports an error. */
+int mla_decode_check(const void* workspace, void* stream);
+
+/* Static English text for a status code. */
+const char* mla_decode_status_string(int status);
+
+/* Introspection for tests and profiling: byte offsets inside a workspace
+ * planned with `num_ranges` (0 = default) of the intermediate buffers
+ *   offsets[0] q_lat  bf16 [B*T*H, 576]   (absorbed query, bf16 part)
+ *   offsets[1] q_lo   bf16 [B*T*H, 512]   (residual q_lat - bf16 part)
+ *   offsets[2] o_lat  bf16 [B*T*H, 512]   (latent attention output)
+ *   offsets[3] plan header (int32 num_ranges, per, total_cost, num_slots)
+ * n must be >= 4.  Not needed for normal use. */
+int mla_decode_workspace_offsets(const mla_decode_dims* dims, int32_t num_ranges,
+                                 int64_t* offsets, int32_t n);
+
+/* Number of kernels one mla_decode_run enqueues (for launch accounting). */
+int mla_decode_kernels_per_run(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_DECODE_H */

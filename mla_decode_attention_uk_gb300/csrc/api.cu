@@ -1,0 +1,361 @@
+// api.cu -- the C ABI declared in include/mla_decode.h: argument validation,
+// workspace layout, TMA descriptor encoding and kernel launches.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mla_decode.h"
+#include "common.cuh"
+
+namespace mla {
+cudaError_t launch_plan(const int32_t* seq_lens, int B, int T, int max_pages, int R,
+                        int32_t* status, PlanHeader* header, int32_t* range_b, int32_t* range_p,
+                        int32_t* seq_first, int32_t* seq_nsplit, int32_t* seq_slot,
+                        int32_t* seq_len_eff, int32_t* prefix, cudaStream_t stream);
+int bmm_token_tile(int BT);
+cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q, int BT, int H,
+                          const __nv_bfloat16* q, __nv_bfloat16* qlat, __nv_bfloat16* qlo,
+                          int32_t* status, cudaStream_t st);
+cudaError_t launch_up_project(const CUtensorMap& tm_wuv, const CUtensorMap& tm_olat, int BT,
+                              int H, __nv_bfloat16* out, int32_t* status, cudaStream_t st);
+int decode_tiles(int T, int H);
+int decode_q_box_rows(int T, int H);
+cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int grid_ctas,
+                          const int32_t* block_table, const int32_t* seq_len_eff,
+                          const PlanHeader* header, void* ws, const int32_t* seq_first,
+                          const int32_t* seq_nsplit, const int32_t* seq_slot,
+                          const __nv_bfloat16* qlo, __nv_bfloat16* olat, float* lse,
+                          int32_t* status, int B, int T, int H, int max_pages,
+                          int num_pages, float scale, cudaStream_t st);
+cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, const void* ws,
+                           const PlanHeader* header, const __nv_bfloat16* qlo,
+                           __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
+                           cudaStream_t st);
+}  // namespace mla
+
+using namespace mla;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];
+std::once_flag g_sm_once[kMaxDevices];
+
+int sm_count(int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return MLA_DECODE_CUDA_ERROR;
+  }
+  std::call_once(g_sm_once[dev], [dev]() {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 0;
+    g_sm_count[dev] = n;
+  });
+  if (g_sm_count[dev] <= 0) {
+    cudaGetLastError();
+    return MLA_DECODE_CUDA_ERROR;
+  }
+  *out = g_sm_count[dev];
+  return MLA_DECODE_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn encoder() {
+  std::call_once(g_encode_once, []() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    else
+      cudaGetLastError();
+  });
+  return g_encode;
+}
+
+// 2-D bf16 tensor map: `rows` x `cols` (row stride `row_stride` elements),
+// box = box_cols x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t row_stride,
+              uint32_t box_cols, uint32_t box_rows, bool stream_hint) {
+  EncodeTiledFn enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_stride * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   stream_hint ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                               : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(const mla_decode_dims* d) {
+  if (!d) return MLA_DECODE_INVALID_ARG;
+  if (d->qk_nope != kNope || d->qk_rope != kRope || d->kv_lora != kLora ||
+      d->v_head != kVHead || d->page_size != kPage)
+    return MLA_DECODE_UNSUPPORTED;
+  if (d->q_len < 1 || d->q_len > 2) return MLA_DECODE_UNSUPPORTED;
+  if (d->num_heads < 16 || d->num_heads > 128 || d->num_heads % 16 != 0)
+    return MLA_DECODE_UNSUPPORTED;
+  if (d->batch < 1 || d->batch > 65535) return MLA_DECODE_INVALID_ARG;
+  if (d->num_pages < 1 || d->max_pages_per_seq < 1) return MLA_DECODE_INVALID_ARG;
+  // Row coordinates of the cache tensor map and key indices are int32.
+  if (static_cast<int64_t>(d->num_pages) * kPage > INT32_MAX) return MLA_DECODE_INVALID_ARG;
+  if (static_cast<int64_t>(d->max_pages_per_seq) * kPage > INT32_MAX / 2)
+    return MLA_DECODE_INVALID_ARG;
+  if (static_cast<int64_t>(d->batch) * d->q_len * d->num_heads > INT32_MAX / kDqk)
+    return MLA_DECODE_INVALID_ARG;
+  return MLA_DECODE_OK;
+}
+
+int default_ranges(const mla_decode_dims* d, int* R) {
+  int sms = 0;
+  int rc = sm_count(&sms);
+  if (rc) return rc;
+  const int tiles = decode_tiles(d->q_len, d->num_heads);
+  *R = sms / tiles > 0 ? sms / tiles : 1;
+  return MLA_DECODE_OK;
+}
+
+// Fixed-offset part of the layout (valid for every R).  The regions sized by
+// the plan's R were checked against the workspace size when the plan was
+// built; kernels locate them from the R recorded in the plan header.
+int layout_for(const mla_decode_dims* d, size_t bytes, WsLayout* L) {
+  *L = make_layout(d->batch, d->q_len, d->num_heads, 1);
+  if (bytes < L->total) return MLA_DECODE_WORKSPACE_TOO_SMALL;
+  return MLA_DECODE_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+int cuda_rc(cudaError_t e) {
+  if (e == cudaSuccess) return MLA_DECODE_OK;
+  cudaGetLastError();
+  return MLA_DECODE_CUDA_ERROR;
+}
+
+int grid_ctas(const mla_decode_dims* d, int* ctas) {
+  int R = 0;
+  int rc = default_ranges(d, &R);
+  if (rc) return rc;
+  *ctas = R * decode_tiles(d->q_len, d->num_heads);
+  return MLA_DECODE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_decode_status_string(int s) {
+  switch (s) {
+    case MLA_DECODE_OK: return "ok";
+    case MLA_DECODE_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad size)";
+    case MLA_DECODE_UNSUPPORTED: return "unsupported configuration (dims or q_len)";
+    case MLA_DECODE_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MLA_DECODE_CUDA_ERROR: return "CUDA error";
+    case MLA_DECODE_DEVICE_BOUNDS: return "block_table entry or seq_len out of range";
+    case MLA_DECODE_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int mla_decode_kernels_per_run(void) { return 4; }
+
+int mla_decode_workspace_size_ex(const mla_decode_dims* d, int32_t num_ranges, size_t* bytes) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!bytes || num_ranges < 0 || num_ranges > 65536) return MLA_DECODE_INVALID_ARG;
+  int R = num_ranges;
+  if (R == 0) {
+    rc = default_ranges(d, &R);
+    if (rc) return rc;
+  }
+  *bytes = make_layout(d->batch, d->q_len, d->num_heads, R).total;
+  return MLA_DECODE_OK;
+}
+
+int mla_decode_workspace_size(const mla_decode_dims* d, size_t* bytes) {
+  return mla_decode_workspace_size_ex(d, 0, bytes);
+}
+
+}  // extern "C"
+
+extern "C" {
+
+int mla_decode_plan_ex(const mla_decode_dims* d, const int32_t* seq_lens, int32_t num_ranges,
+                       void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!seq_lens || !ws || !aligned16(ws) || num_ranges < 0 || num_ranges > 65536)
+    return MLA_DECODE_INVALID_ARG;
+  int R = num_ranges;
+  if (R == 0) {
+    rc = default_ranges(d, &R);
+    if (rc) return rc;
+  }
+  const WsLayout L = make_layout(d->batch, d->q_len, d->num_heads, R);
+  if (ws_bytes < L.total) return MLA_DECODE_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(at<int32_t>(ws, L.status), 0, sizeof(int32_t), st) != cudaSuccess)
+    return cuda_rc(cudaErrorUnknown);
+  return cuda_rc(launch_plan(seq_lens, d->batch, d->q_len, d->max_pages_per_seq, R,
+                             at<int32_t>(ws, L.status), at<PlanHeader>(ws, L.header),
+                             at<int32_t>(ws, L.range_b), at<int32_t>(ws, L.range_p),
+                             at<int32_t>(ws, L.seq_first), at<int32_t>(ws, L.seq_nsplit),
+                             at<int32_t>(ws, L.seq_slot), at<int32_t>(ws, L.seq_len_eff),
+                             at<int32_t>(ws, L.prefix), st));
+}
+
+int mla_decode_plan(const mla_decode_dims* d, const int32_t* seq_lens, void* ws, size_t ws_bytes,
+                    void* stream) {
+  return mla_decode_plan_ex(d, seq_lens, 0, ws, ws_bytes, stream);
+}
+
+int mla_decode_absorb(const mla_decode_dims* d, const void* q, const void* w_uk, void* ws,
+                      size_t ws_bytes, void* stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!q || !w_uk || !ws || !aligned16(q) || !aligned16(w_uk) || !aligned16(ws))
+    return MLA_DECODE_INVALID_ARG;
+  WsLayout L;
+  rc = layout_for(d, ws_bytes, &L);
+  if (rc) return rc;
+  const int BT = d->batch * d->q_len, H = d->num_heads;
+  CUtensorMap tm_q, tm_w;
+  if (!make_map(&tm_q, q, BT, static_cast<uint64_t>(H) * kDq, static_cast<uint64_t>(H) * kDq,
+                kBoxCols, bmm_token_tile(BT), false) ||
+      !make_map(&tm_w, w_uk, static_cast<uint64_t>(H) * kNope, kLora, kLora, kBoxCols, 64, false))
+    return MLA_DECODE_CUDA_ERROR;
+  return cuda_rc(launch_absorb(tm_w, tm_q, BT, H, static_cast<const __nv_bfloat16*>(q),
+                               at<__nv_bfloat16>(ws, L.qlat), at<__nv_bfloat16>(ws, L.qlo),
+                               at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream)));
+}
+
+int mla_decode_attend(const mla_decode_dims* d, const void* kv_cache, const int32_t* block_table,
+                      const int32_t* seq_lens, float scale, float* lse, void* ws, size_t ws_bytes,
+                      void* stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!kv_cache || !block_table || !seq_lens || !lse || !ws || !aligned16(kv_cache) ||
+      !aligned16(ws) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return MLA_DECODE_INVALID_ARG;
+  WsLayout L;
+  rc = layout_for(d, ws_bytes, &L);
+  if (rc) return rc;
+  const int TH = d->q_len * d->num_heads;
+  const uint64_t rows = static_cast<uint64_t>(d->batch) * TH;
+  CUtensorMap tm_q, tm_c;
+  if (!make_map(&tm_q, at<void>(ws, L.qlat), rows, kDqk, kDqk, kBoxCols,
+                decode_q_box_rows(d->q_len, d->num_heads), false) ||
+      !make_map(&tm_c, kv_cache, static_cast<uint64_t>(d->num_pages) * kPage, kDqk, kDqk,
+                kBoxCols, kPage, true))
+    return MLA_DECODE_CUDA_ERROR;
+  int ctas = 0;
+  rc = grid_ctas(d, &ctas);
+  if (rc) return rc;
+  return cuda_rc(launch_decode(
+      tm_q, tm_c, ctas, block_table, at<int32_t>(ws, L.seq_len_eff), at<PlanHeader>(ws, L.header),
+      ws, at<int32_t>(ws, L.seq_first), at<int32_t>(ws, L.seq_nsplit), at<int32_t>(ws, L.seq_slot),
+      at<__nv_bfloat16>(ws, L.qlo), at<__nv_bfloat16>(ws, L.olat), lse,
+      at<int32_t>(ws, L.status), d->batch, d->q_len, d->num_heads, d->max_pages_per_seq,
+      d->num_pages, scale, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_decode_combine(const mla_decode_dims* d, float scale, float* lse, void* ws,
+                       size_t ws_bytes, void* stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!lse || !ws || !aligned16(ws) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return MLA_DECODE_INVALID_ARG;
+  WsLayout L;
+  rc = layout_for(d, ws_bytes, &L);
+  if (rc) return rc;
+  return cuda_rc(launch_combine(at<int32_t>(ws, L.seq_nsplit), at<int32_t>(ws, L.seq_slot), ws,
+                                at<PlanHeader>(ws, L.header), at<__nv_bfloat16>(ws, L.qlo),
+                                at<__nv_bfloat16>(ws, L.olat), lse, d->batch, d->q_len,
+                                d->num_heads, scale, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_decode_up_project(const mla_decode_dims* d, const void* w_uv, void* out, void* ws,
+                          size_t ws_bytes, void* stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!w_uv || !out || !ws || !aligned16(w_uv) || !aligned16(out) || !aligned16(ws))
+    return MLA_DECODE_INVALID_ARG;
+  WsLayout L;
+  rc = layout_for(d, ws_bytes, &L);
+  if (rc) return rc;
+  const int BT = d->batch * d->q_len, H = d->num_heads;
+  CUtensorMap tm_o, tm_w;
+  if (!make_map(&tm_o, at<void>(ws, L.olat), BT, static_cast<uint64_t>(H) * kLora,
+                static_cast<uint64_t>(H) * kLora, kBoxCols, bmm_token_tile(BT), false) ||
+      !make_map(&tm_w, w_uv, static_cast<uint64_t>(H) * kLora, kVHead, kVHead, kBoxCols, 64,
+                false))
+    return MLA_DECODE_CUDA_ERROR;
+  return cuda_rc(launch_up_project(tm_w, tm_o, BT, H, static_cast<__nv_bfloat16*>(out),
+                                   at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream)));
+}
+
+int mla_decode_run(const mla_decode_dims* d, const void* q, const void* kv_cache,
+                   const int32_t* block_table, const int32_t* seq_lens, const void* w_uk,
+                   const void* w_uv, float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                   void* stream) {
+  int rc = mla_decode_absorb(d, q, w_uk, ws, ws_bytes, stream);
+  if (rc) return rc;
+  rc = mla_decode_attend(d, kv_cache, block_table, seq_lens, scale, lse, ws, ws_bytes, stream);
+  if (rc) return rc;
+  rc = mla_decode_combine(d, scale, lse, ws, ws_bytes, stream);
+  if (rc) return rc;
+  return mla_decode_up_project(d, w_uv, out, ws, ws_bytes, stream);
+}
+
+int mla_decode_workspace_offsets(const mla_decode_dims* d, int32_t num_ranges,
+                                 int64_t* offsets, int32_t n) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!offsets || n < 4 || num_ranges < 0 || num_ranges > 65536) return MLA_DECODE_INVALID_ARG;
+  int R = num_ranges;
+  if (R == 0) {
+    rc = default_ranges(d, &R);
+    if (rc) return rc;
+  }
+  const WsLayout L = make_layout(d->batch, d->q_len, d->num_heads, R);
+  offsets[0] = static_cast<int64_t>(L.qlat);
+  offsets[1] = static_cast<int64_t>(L.qlo);
+  offsets[2] = static_cast<int64_t>(L.olat);
+  offsets[3] = static_cast<int64_t>(L.header);
+  return MLA_DECODE_OK;
+}
+
+int mla_decode_check(const void* ws, void* stream) {
+  if (!ws) return MLA_DECODE_INVALID_ARG;
+  int32_t host = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The status word sits at offset 0 of every layout.
+  if (cudaMemcpyAsync(&host, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return cuda_rc(cudaErrorUnknown);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_rc(cudaErrorUnknown);
+  return host;
+}
+
+}  // extern "C"

@@ -1,0 +1,220 @@
+// bmm.cu -- steps a2 and a5: the two per-head bf16 batched matmuls that
+// replace materialised absorbed weights (vLLM PR #14770 "[Attention] MLA get
+// rid of materialization", PR description: sequential bf16 matmuls with W_UK
+// before attention and W_UV after it).
+//
+//   absorb (a2):      q_lat[tok, h, 0:512] = q_nope[tok, h, :] . W_UK[h]   (K = 128)
+//                     q_lat[tok, h, 512:576] = q_pe[tok, h, :]
+//   up-project (a5):  out[tok, h, :] = o_lat[tok, h, :] . W_UV[h]          (K = 512)
+//
+// Both run transposed on the tensor cores so the weight dimension fills the
+// 128-row MMA and the (often small) token count is the N dimension:
+//   D[m, tok] = sum_k W[h][k][m] * X[tok, h, k]
+// A = a 128-wide slice of W[h] (MN-major, staged by TMA with 128B swizzle),
+// B = a token tile of X (K-major), D in TMEM (fp32), one CTA per
+// (token tile, 128-wide m block, head).  Warp 0 issues TMA, warp 1 issues the
+// MMAs, warp 2 owns TMEM, and all four warps run the epilogue.
+//
+// The absorb epilogue also writes the bf16 residual q_lat - bf16(q_lat), which
+// the attention step uses to correct its log-sum-exp to first order.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kBmmThreads = 128;
+constexpr int kStages = 4;
+constexpr int kABytes = 2 * kBoxBytes;  // 128 m x 64 k, two 64-wide m boxes
+
+enum class BmmMode { kAbsorb, kUpProject };
+
+template <int NT>
+struct BmmSmem {
+  static constexpr int kBBytes = NT * 128;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTotal = kStages * kStageBytes + 1024;  // + alignment slack
+};
+
+template <BmmMode MODE, int NT>
+__global__ void __launch_bounds__(kBmmThreads)
+bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+           int BT, int H, int K, int Kx, const __nv_bfloat16* __restrict__ q,
+           __nv_bfloat16* __restrict__ out_hi, __nv_bfloat16* __restrict__ out_lo,
+           int32_t* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], done_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tok0 = blockIdx.x * NT;
+  const int m0 = blockIdx.y * 128;
+  const int h = blockIdx.z;
+  const int nk = K / 64;
+  constexpr uint32_t kTmemCols = NT < 32 ? 32 : NT;
+  using S = BmmSmem<NT>;
+
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    mbar_init(smem_u32(&done_bar), 1);
+    abort_sh = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_x);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    if (elect_one()) {
+      for (int kc = 0; kc < nk; ++kc) {
+        const int s = kc % kStages;
+        if (kc >= kStages &&
+            !mbar_wait(smem_u32(&empty_bar[s]), ((kc / kStages) - 1) & 1, &abort_sh, status))
+          break;
+        const uint32_t a = sbase + s * S::kStageBytes;
+        const uint32_t b = a + kABytes;
+        const uint32_t fb = smem_u32(&full_bar[s]);
+        mbar_expect_tx(fb, S::kStageBytes);
+        tma_load_2d(a, &tm_w, m0, h * K + kc * 64, fb);
+        tma_load_2d(a + kBoxBytes, &tm_w, m0 + 64, h * K + kc * 64, fb);
+        tma_load_2d(b, &tm_x, h * Kx + kc * 64, tok0, fb);
+      }
+    }
+  } else if (warp == 1) {
+    if (elect_one()) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, NT, /*a_mn=*/true, /*b_mn=*/false);
+      bool ok = true;
+      for (int kc = 0; kc < nk && ok; ++kc) {
+        const int s = kc % kStages;
+        if (!mbar_wait(smem_u32(&full_bar[s]), (kc / kStages) & 1, &abort_sh, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a = sbase + s * S::kStageBytes;
+        const uint32_t b = a + kABytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = sdesc_sw128(a + kk * 2048, kBoxBytes, 1024);
+          const uint64_t bd = sdesc_sw128(b + kk * 32, 16, 1024);
+          umma_bf16(tmem, ad, bd, idesc, (kc | kk) != 0);
+        }
+        umma_commit(smem_u32(&empty_bar[s]));
+      }
+      umma_commit(smem_u32(&done_bar));
+    }
+  }
+  __syncwarp();
+
+  // Epilogue: thread (warp w, lane i) owns output feature m0 + 32 w + i.
+  const bool have = mbar_wait(smem_u32(&done_bar), 0, &abort_sh, status);
+  tc_fence_after();
+  const int m = m0 + warp * 32 + lane;
+  if (have && !abort_sh) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < NT; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int tok = tok0 + c0 + j;
+        if (tok >= BT) break;
+        const float v = __uint_as_float(r[j]);
+        const size_t row = static_cast<size_t>(tok) * H + h;
+        if constexpr (MODE == BmmMode::kAbsorb) {
+          const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+          out_hi[row * kDqk + m] = hi;
+          out_lo[row * kLora + m] = __float2bfloat16_rn(v - __bfloat162float(hi));
+        } else {
+          out_hi[row * kVHead + m] = __float2bfloat16_rn(v);
+        }
+      }
+    }
+    if constexpr (MODE == BmmMode::kAbsorb) {
+      // q_pe passes through unchanged into columns 512..575.
+      if (blockIdx.y == 0) {
+        for (int i = threadIdx.x; i < NT * (kRope / 2); i += kBmmThreads) {
+          const int tok = tok0 + i / (kRope / 2);
+          const int c = (i % (kRope / 2)) * 2;
+          if (tok < BT) {
+            const size_t row = static_cast<size_t>(tok) * H + h;
+            const uint32_t v =
+                *reinterpret_cast<const uint32_t*>(q + row * kDq + kNope + c);
+            *reinterpret_cast<uint32_t*>(out_hi + row * kDqk + kLora + c) = v;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <BmmMode MODE, int NT>
+cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, int H, int K,
+                          int Kx, int Mtot, const __nv_bfloat16* q, __nv_bfloat16* hi,
+                          __nv_bfloat16* lo, int32_t* status, cudaStream_t st) {
+  auto kern = bmm_kernel<MODE, NT>;
+  const int smem = BmmSmem<NT>::kTotal;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((BT + NT - 1) / NT, Mtot / 128, H);
+  kern<<<grid, kBmmThreads, smem, st>>>(tw, tx, BT, H, K, Kx, q, hi, lo, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Token tile used for a given token count (also the TMA box height of X).
+int bmm_token_tile(int BT) {
+  if (BT <= 16) return 16;
+  if (BT <= 32) return 32;
+  if (BT <= 64) return 64;
+  return 128;
+}
+
+cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q, int BT, int H,
+                          const __nv_bfloat16* q, __nv_bfloat16* qlat, __nv_bfloat16* qlo,
+                          int32_t* status, cudaStream_t st) {
+  switch (bmm_token_tile(BT)) {
+    case 16: return launch_bmm_nt<BmmMode::kAbsorb, 16>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st);
+    case 32: return launch_bmm_nt<BmmMode::kAbsorb, 32>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st);
+    case 64: return launch_bmm_nt<BmmMode::kAbsorb, 64>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st);
+    default: return launch_bmm_nt<BmmMode::kAbsorb, 128>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st);
+  }
+}
+
+cudaError_t launch_up_project(const CUtensorMap& tm_wuv, const CUtensorMap& tm_olat, int BT,
+                              int H, __nv_bfloat16* out, int32_t* status, cudaStream_t st) {
+  switch (bmm_token_tile(BT)) {
+    case 16: return launch_bmm_nt<BmmMode::kUpProject, 16>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st);
+    case 32: return launch_bmm_nt<BmmMode::kUpProject, 32>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st);
+    case 64: return launch_bmm_nt<BmmMode::kUpProject, 64>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st);
+    default: return launch_bmm_nt<BmmMode::kUpProject, 128>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st);
+  }
+}
+
+}  // namespace mla

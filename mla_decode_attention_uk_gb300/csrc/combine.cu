@@ -1,0 +1,103 @@
+// combine.cu -- step a4: merge split-KV partial results by log-sum-exp.
+//
+// A sequence cut into n key ranges has, per query row, n latent outputs o_s
+// (each normalised over its own range) and their log-sum-exps lse_s.  Softmax
+// over the union of the ranges is the lse-weighted mixture:
+//   lse = ln sum_s exp(lse_s),   o = sum_s exp(lse_s - lse) o_s,
+// the split-KV decomposition of the FlashAttention family that FlashMLA
+// credits ("DeepSeek publica FlashMLA como codigo abierto").  The merged o is
+// stored as bf16 o_lat for the W_UV bmm; lse gets the first-order correction
+// scale * (q_lo . o) for the bf16 rounding of the absorbed query.
+// One warp per query row; each lane owns 16 of the 512 latent columns and
+// moves them with 16-byte vector loads and 8-byte vector stores.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kCombThreads = 256;
+constexpr int kRowsPerCta = kCombThreads / 32;
+
+__global__ void __launch_bounds__(kCombThreads)
+combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict__ seq_slot,
+               const uint8_t* __restrict__ ws, const PlanHeader* __restrict__ header, int B,
+               int T, int H, const __nv_bfloat16* __restrict__ qlo,
+               __nv_bfloat16* __restrict__ olat, float* __restrict__ lse_out, float scale) {
+  const int TH = T * H;
+  const int b = blockIdx.y;
+  const int r = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int ns = seq_nsplit[b];
+  if (ns <= 1 || r >= TH) return;
+  const int slot0 = seq_slot[b];
+  const WsLayout L = make_layout(B, T, H, header->num_ranges);
+  const float* __restrict__ opart = reinterpret_cast<const float*>(ws + L.opart);
+  const float* __restrict__ lpart = reinterpret_cast<const float*>(ws + L.lpart);
+
+  float m = -INFINITY;
+  for (int s = 0; s < ns; ++s) m = fmaxf(m, lpart[static_cast<size_t>(slot0 + s) * TH + r]);
+  float wsum = 0.0f;
+  for (int s = 0; s < ns; ++s) {
+    const float l = lpart[static_cast<size_t>(slot0 + s) * TH + r];
+    wsum += (l == -INFINITY) ? 0.0f : __expf(l - m);
+  }
+  const float lse = m + __logf(wsum);
+
+  float4 acc[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < ns; ++s) {
+    const float l = lpart[static_cast<size_t>(slot0 + s) * TH + r];
+    const float w = (l == -INFINITY) ? 0.0f : __expf(l - lse);
+    const float4* src =
+        reinterpret_cast<const float4*>(opart + (static_cast<size_t>(slot0 + s) * TH + r) * kLora);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 v = src[q * 32 + lane];
+      acc[q].x += w * v.x;
+      acc[q].y += w * v.y;
+      acc[q].z += w * v.z;
+      acc[q].w += w * v.w;
+    }
+  }
+
+  const size_t row = static_cast<size_t>(b) * TH + r;
+  float corr = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int col = (q * 32 + lane) * 4;
+    const uint2 lo_raw = *reinterpret_cast<const uint2*>(qlo + row * kLora + col);
+    const __nv_bfloat162 l01 = *reinterpret_cast<const __nv_bfloat162*>(&lo_raw.x);
+    const __nv_bfloat162 l23 = *reinterpret_cast<const __nv_bfloat162*>(&lo_raw.y);
+    corr += __low2float(l01) * acc[q].x + __high2float(l01) * acc[q].y +
+            __low2float(l23) * acc[q].z + __high2float(l23) * acc[q].w;
+    __nv_bfloat162 o01 = __floats2bfloat162_rn(acc[q].x, acc[q].y);
+    __nv_bfloat162 o23 = __floats2bfloat162_rn(acc[q].z, acc[q].w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t*>(&o01);
+    packed.y = *reinterpret_cast<uint32_t*>(&o23);
+    *reinterpret_cast<uint2*>(olat + row * kLora + col) = packed;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) corr += __shfl_xor_sync(0xffffffffu, corr, o);
+  if (lane == 0) lse_out[row] = lse + scale * corr;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, const void* ws,
+                           const PlanHeader* header, const __nv_bfloat16* qlo,
+                           __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
+                           cudaStream_t st) {
+  dim3 grid((T * H + kRowsPerCta - 1) / kRowsPerCta, B);
+  combine_kernel<<<grid, kCombThreads, 0, st>>>(seq_nsplit, seq_slot,
+                                                static_cast<const uint8_t*>(ws), header, B, T, H,
+                                                qlo, olat, lse, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

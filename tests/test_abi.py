@@ -1,0 +1,107 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point declared in include/mla_decode.h, and rejects bad arguments
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mla_decode_attention_uk_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mla_decode.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|int)\s+(mla_decode_\w+)\s*\(", src,
+                                 flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    fns = declared_functions()
+    for must in ("mla_decode_workspace_size", "mla_decode_plan", "mla_decode_run",
+                 "mla_decode_check", "mla_decode_status_string"):
+        assert must in fns
+
+
+def test_library_exports_every_declared_symbol():
+    L = binding.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert set(declared_functions()) == set(binding.ENTRY_POINTS)
+
+
+def test_library_links_no_torch_and_no_cuda_driver_at_load():
+    # dlopen works on a machine without a GPU driver: the runtime is static and
+    # the driver is resolved lazily.
+    with open(binding.LIB_PATH, "rb") as f:
+        head = f.read()
+    assert b"libtorch" not in head and b"libc10" not in head
+
+
+def test_status_strings():
+    L = binding.lib()
+    for code in range(7):
+        s = L.mla_decode_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert L.mla_decode_status_string(99).decode() == "unknown status"
+    assert L.mla_decode_kernels_per_run() == 4
+
+
+def good_dims(**kw):
+    d = dict(batch=2, q_len=1, num_heads=16, qk_nope=128, qk_rope=64, kv_lora=512, v_head=128,
+             page_size=64, num_pages=4, max_pages_per_seq=2)
+    d.update(kw)
+    return binding.Dims(**d)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("qk_nope", 64, 2), ("qk_rope", 32, 2), ("kv_lora", 256, 2), ("v_head", 64, 2),
+    ("page_size", 16, 2), ("q_len", 3, 2), ("q_len", 0, 2), ("num_heads", 8, 2),
+    ("num_heads", 24, 2), ("num_heads", 256, 2), ("batch", 0, 1), ("num_pages", 0, 1),
+    ("max_pages_per_seq", 0, 1),
+])
+def test_bad_dims_rejected_on_host(field, value, code):
+    L = binding.lib()
+    n = ctypes.c_size_t(0)
+    d = good_dims(**{field: value})
+    assert L.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == code
+    assert L.mla_decode_plan(ctypes.byref(d), None, None, 0, None) == code
+
+
+def test_null_pointers_rejected_before_any_launch():
+    L = binding.lib()
+    d = good_dims()
+    fake = ctypes.c_void_p(4096)
+    assert L.mla_decode_workspace_size(None, None) == 1
+    assert L.mla_decode_workspace_size(ctypes.byref(d), None) == 1
+    assert L.mla_decode_plan(ctypes.byref(d), None, fake, 1 << 20, None) == 1
+    assert L.mla_decode_plan(ctypes.byref(d), fake, None, 1 << 20, None) == 1
+    assert L.mla_decode_run(ctypes.byref(d), None, fake, fake, fake, fake, fake,
+                            ctypes.c_float(0.07), fake, fake, fake, 1 << 20, None) == 1
+    assert L.mla_decode_absorb(ctypes.byref(d), fake, None, fake, 1 << 20, None) == 1
+    assert L.mla_decode_attend(ctypes.byref(d), fake, None, fake, ctypes.c_float(0.07), fake,
+                               fake, 1 << 20, None) == 1
+    assert L.mla_decode_combine(ctypes.byref(d), ctypes.c_float(0.07), None, fake, 1 << 20,
+                                None) == 1
+    assert L.mla_decode_up_project(ctypes.byref(d), fake, None, fake, 1 << 20, None) == 1
+    assert L.mla_decode_check(None, None) == 1
+
+
+def test_misaligned_pointers_rejected():
+    L = binding.lib()
+    d = good_dims()
+    ok, bad = ctypes.c_void_p(4096), ctypes.c_void_p(4096 + 2)
+    assert L.mla_decode_absorb(ctypes.byref(d), bad, ok, ok, 1 << 30, None) == 1
+    assert L.mla_decode_absorb(ctypes.byref(d), ok, ok, bad, 1 << 30, None) == 1
+    assert L.mla_decode_up_project(ctypes.byref(d), ok, bad, ok, 1 << 30, None) == 1
+
+
+def test_workspace_too_small_rejected_before_launch():
+    L = binding.lib()
+    d = good_dims()
+    ok = ctypes.c_void_p(4096)
+    assert L.mla_decode_absorb(ctypes.byref(d), ok, ok, ok, 64, None) == 3
+    assert L.mla_decode_combine(ctypes.byref(d), ctypes.c_float(0.07), ok, ok, 64, None) == 3

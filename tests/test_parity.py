@@ -1,0 +1,132 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances: max |d out| <= 2e-2, mean |d out| <= 2e-3, max |d lse| <= 1e-3.
+Small cases compare every output; full-size workloads compare sampled rows the
+oracle computes one by one."""
+import math
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_decode_attention_uk_gb300 import binding
+from mla_decode_attention_uk_gb300.inputs import make_inputs, workload_inputs
+
+from parity_util import assert_parity, compare, run_gpu, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def test_absorb_bmm_matches_fp32_matmul():
+    inp = make_inputs(3, [70, 5, 300], 2, 32, seed=41)
+    dev = torch.device("cuda")
+    g = inp.to(dev)
+    d = binding.dims_for(g.q, g.cache, g.block_table)
+    m = binding.MlaDecode(d, dev)
+    m.absorb(g.q, g.w_uk)
+    torch.cuda.synchronize()
+    hi = m.q_lat().float().cpu()
+    lo = m.q_lo().float().cpu()
+    ref = torch.einsum("bthk,hkl->bthl", inp.q[..., :128].double(), inp.w_uk.double())
+    ref = ref.reshape(-1, 512)
+    got = hi[:, :512].double() + lo.double()
+    assert (got - ref).abs().max().item() < 2e-5
+    assert torch.equal(hi[:, 512:], inp.q[..., 128:].reshape(-1, 64).float())
+    # hi is the bf16 rounding of the fp32 product, lo the bf16 rounding of the rest
+    assert (hi[:, :512].double() - ref).abs().max().item() <= ref.abs().max().item() * 2 ** -8
+
+
+def test_tiny_workload_all_rows():
+    inp = workload_inputs("tiny")
+    out, lse, _ = run_gpu(inp)
+    assert_parity(compare(inp, out, lse), "tiny")
+
+
+@pytest.mark.parametrize("H,T", [(16, 1), (32, 1), (64, 1), (128, 1), (16, 2), (64, 2), (128, 2)])
+def test_ragged_lengths_all_rows(H, T):
+    lens = [T, 1 + T, 63, 64, 65, 127, 128, 129, 200, 511, 700]
+    inp = make_inputs(len(lens), lens, T, H, seed=100 + H + T)
+    out, lse, _ = run_gpu(inp)
+    assert_parity(compare(inp, out, lse), "H=%d T=%d" % (H, T))
+
+
+@pytest.mark.parametrize("num_ranges", [1, 3, 7, 64, 300, 1000])
+def test_split_counts(num_ranges):
+    lens = [5, 700, 64, 1300, 2, 333]
+    inp = make_inputs(len(lens), lens, 2, 16, seed=7)
+    out, lse, m = run_gpu(inp, num_ranges=num_ranges)
+    hdr = m.plan_header()
+    assert hdr[0] == num_ranges
+    assert_parity(compare(inp, out, lse), "R=%d" % num_ranges)
+
+
+def test_split_counts_h128():
+    lens = [900, 2000, 70]
+    inp = make_inputs(len(lens), lens, 1, 128, seed=8)
+    for R in (2, 41):
+        out, lse, _ = run_gpu(inp, num_ranges=R)
+        assert_parity(compare(inp, out, lse), "R=%d" % R)
+
+
+def test_deterministic_for_a_fixed_plan():
+    inp = make_inputs(4, [100, 1000, 64, 2000], 1, 64, seed=9)
+    o1, l1, _ = run_gpu(inp, num_ranges=5)
+    o2, l2, _ = run_gpu(inp, num_ranges=5)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_page_permutation_same_schedule_bitwise():
+    inp = make_inputs(3, [130, 640, 77], 1, 32, seed=10)
+    o1, l1, _ = run_gpu(inp)
+    g = torch.Generator().manual_seed(5)
+    perm = torch.randperm(inp.cache.shape[0], generator=g)
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(perm.numel())
+    inp.cache = inp.cache[perm].contiguous()
+    valid = inp.block_table >= 0
+    inp.block_table[valid] = inv[inp.block_table[valid].long()].to(torch.int32)
+    o2, l2, _ = run_gpu(inp)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_unreferenced_nan_pages_do_not_leak():
+    inp = make_inputs(3, [100, 31, 64], 1, 16, seed=11, spare_pages=4)
+    out, lse, _ = run_gpu(inp)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    assert_parity(compare(inp, out, lse), "nan spare")
+
+
+def test_single_key_closed_form():
+    inp = make_inputs(2, [1, 1], 1, 16, seed=12)
+    out, lse, _ = run_gpu(inp)
+    assert_parity(compare(inp, out, lse), "L=1")
+
+
+def test_bad_block_table_entry_sets_status_without_fault():
+    inp = make_inputs(2, [100, 100], 1, 16, seed=13)
+    inp.block_table[1, 1] = inp.cache.shape[0] + 5
+    out, lse, m = run_gpu(inp, check_status=False)
+    assert m.check() == 5
+    # the other sequence is still right
+    st = compare(inp.__class__(inp.q[:1].clone(), inp.cache, inp.block_table[:1].clone(),
+                               inp.seq_lens[:1].clone(), inp.w_uk, inp.w_uv, inp.scale),
+                 out[:1], lse[:1])
+    assert_parity(st, "valid sequence next to a bad one")
+
+
+def test_seq_len_beyond_block_table_sets_status():
+    inp = make_inputs(2, [100, 100], 1, 16, seed=14)
+    inp.seq_lens[0] = inp.block_table.shape[1] * 64 + 1
+    _, _, m = run_gpu(inp, check_status=False)
+    assert m.check() == 5
+
+
+@pytest.mark.parametrize("name", ["tp_shard", "full_head", "long", "mixed_spec"])
+def test_full_size_workloads_sampled(name):
+    inp = workload_inputs(name)
+    out, lse, _ = run_gpu(inp)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    rows = sample_rows(inp, 96, seed=1)
+    assert_parity(compare(inp, out, lse, rows=rows), name)
