@@ -1,0 +1,434 @@
+"""Benchmark: MLA decode (weight-absorbed, paged latent cache) on GB300.
+
+One step = one pass of the whole hot path over one decode batch: plan
+(split-KV partition) + q-absorb bmm + split-KV latent attention + LSE combine
++ W_UV bmm, all through the C ABI of libmla_decode.so, inputs resident in HBM.
+
+Prints ONE JSON line (rank 0).  value = latent-cache GB/s (1152 B per cached
+token per sequence, read once per step) summed over all ranks.  Also reports
+TFLOP/s (2176 FLOP per query row and key + the two bmms) and decode tokens/s,
+the roofline of the dominant kernel (the attention step) against the measured
+HBM copy bandwidth, an end-to-end figure through the same C ABI with host
+buffers, and the fp64 CPU oracle timed on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+N > 1 runs under torch.distributed.run, one independent replica per GPU
+(the path needs no exchange between GPUs: weak scaling).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from mla_decode_attention_uk_gb300.inputs import WORKLOADS, workload_inputs  # noqa: E402
+
+METRIC = "MLA decode latent-KV GB/s, TFLOPS & tokens/s vs GB300 roofline (1 GPU)"
+DEFAULT_WORKLOAD = "tp_shard"
+BYTES_PER_TOKEN = 1152          # 576 bf16 per cached token
+FLOP_PER_ROW_KEY = 2 * (576 + 512)
+FLOP_PER_ROW_BMM = 2 * 2 * 128 * 512
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def decode_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode.cu", "ptx.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "mla_decode_attention_uk_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per attention launch from the committed ncu summary, if the
+    kernel source is unchanged since the capture; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_hash") != decode_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def workload_stats(inp):
+    B, T, H = inp.q.shape[:3]
+    sum_len = int(inp.seq_lens.sum())
+    rows_keys = 0
+    for L in inp.seq_lens.tolist():
+        for t in range(T):
+            rows_keys += H * (L - T + t + 1)
+    cache_bytes = BYTES_PER_TOKEN * sum_len
+    weight_bytes = H * 2 * (128 * 512 * 2)
+    flops = FLOP_PER_ROW_KEY * rows_keys + FLOP_PER_ROW_BMM * B * T * H
+    return dict(B=B, T=T, H=H, sum_len=sum_len, cache_bytes=cache_bytes,
+                weight_bytes=weight_bytes, flops=flops, tokens=B * T)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def _one(self):
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                               timeout=10)
+            for line in r.stdout.strip().splitlines():
+                self.rows.append([x.strip() for x in line.split(",")])
+        except Exception:
+            pass
+
+    def start(self):
+        self._one()
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index),
+                                          "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=10)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            for line in out.strip().splitlines():
+                self.rows.append([x.strip() for x in line.split(",")])
+        self._one()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample(inp_cpu, budget_s):
+    """Pick a bounded sample of query rows for the fp64 oracle: whole leading
+    sequences while they fit the budget, else the first rows of sequence 0.
+    Each sequence's cache bytes (and its tokens) are attributed evenly to its
+    T*H query rows, so the sample's throughput is in the workload's units.
+    Returns (rows or None, sample bytes, sample flops, sample tokens, text)."""
+    import oracle
+    B, T, H = inp_cpu.q.shape[:3]
+    TH = T * H
+    lens = inp_cpu.seq_lens.tolist()
+    # calibrate on a few rows of sequence 0
+    probe = list(range(min(TH, 4)))
+    t0 = time.perf_counter()
+    oracle.decode(inp_cpu.q, inp_cpu.cache, inp_cpu.block_table, inp_cpu.seq_lens, inp_cpu.w_uk,
+                  inp_cpu.w_uv, inp_cpu.scale, rows=probe)
+    per_row = (time.perf_counter() - t0) / len(probe) / max(1, lens[0])  # s per row-key
+    par = max(1, oracle.threads())
+    rows, keys = [], 0
+    for b in range(B):
+        for r in range(TH):
+            rows.append(b * TH + r)
+            keys += lens[b]
+            if keys * per_row / par >= budget_s:
+                break
+        else:
+            continue
+        break
+    nbytes = sum(BYTES_PER_TOKEN * lens[row // TH] / TH for row in rows)
+    flops = sum(FLOP_PER_ROW_KEY * (lens[row // TH] - T + (row % TH) // H + 1) + FLOP_PER_ROW_BMM
+                for row in rows)
+    tokens = len(rows) / H
+    text = "%d query rows (first %d sequence(s)) of %d; cache bytes attributed per row" % (
+        len(rows), rows[-1] // TH + 1, B * TH)
+    return rows, nbytes, flops, tokens, text
+
+
+def time_oracle(inp_cpu, budget_s):
+    import oracle
+    rows, nbytes, flops, tokens, text = oracle_sample(inp_cpu, budget_s)
+    t0 = time.perf_counter()
+    oracle.decode(inp_cpu.q, inp_cpu.cache, inp_cpu.block_table, inp_cpu.seq_lens, inp_cpu.w_uk,
+                  inp_cpu.w_uv, inp_cpu.scale, rows=rows)
+    dt = time.perf_counter() - t0
+    return dt, nbytes, flops, tokens, text
+
+
+def dist_setup(n_gpus):
+    if n_gpus > 1 or "RANK" in os.environ:
+        import torch.distributed as dist
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return rank, world, local, dist
+    return 0, 1, 0, None
+
+
+def run_reference(args):
+    """The reference arm: the fp64 CPU oracle as it stands, on the host cores,
+    each step a bounded row sample of the same workload."""
+    rank, world, local, dist = dist_setup(args.gpus)
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    import oracle
+    inp = workload_inputs(args.workload)
+    budget = min(1.0, 120.0 / max(1, args.steps + args.warmup))
+    rows, nbytes, flops, tokens, text = oracle_sample(inp, budget)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.decode(inp.q, inp.cache, inp.block_table, inp.seq_lens, inp.w_uk, inp.w_uv,
+                      inp.scale, rows=rows)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    per_step = sum(times) / len(times)
+    value = nbytes / per_step / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "note": WORKLOADS[args.workload].note},
+        "tflops": flops / per_step / 1e12, "tokens_per_s": tokens / per_step,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": text},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch every step from the host")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    from mla_decode_attention_uk_gb300 import binding
+    rank, world, local, dist = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    inp_cpu = workload_inputs(args.workload)
+    stats = workload_stats(inp_cpu)
+    g = inp_cpu.to(dev)
+    d = binding.dims_for(g.q, g.cache, g.block_table)
+    m = binding.MlaDecode(d, dev)
+    B, T, H = stats["B"], stats["T"], stats["H"]
+    out = torch.empty(B, T, H, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, T, H, dtype=torch.float32, device=dev)
+
+    def step():
+        m.plan(g.seq_lens)
+        m.absorb(g.q, g.w_uk)
+        m.attend(g.cache, g.block_table, g.seq_lens, g.scale, lse)
+        m.combine(g.scale, lse)
+        m.up_project(g.w_uv, out)
+
+    def attend_only():
+        m.attend(g.cache, g.block_table, g.seq_lens, g.scale, lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = m.check()
+    if st != 0:
+        raise SystemExit("device status %d after warm-up" % st)
+
+    # The step is launch-bound on the host for small batches: capture it once
+    # in a CUDA graph and replay it (same kernels, same arguments).
+    graph_step = graph_attend = None
+    if not args.no_graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+            attend_only()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph_step, graph_attend = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_step):
+            step()
+        with torch.cuda.graph(graph_attend):
+            attend_only()
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            graph_step.replay()
+        torch.cuda.synchronize()
+    run_step = graph_step.replay if graph_step is not None else step
+    run_attend = graph_attend.replay if graph_attend is not None else attend_only
+
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    t_start.record(stream)
+    for i in range(args.steps):
+        run_step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks.stop()
+    st = m.check()
+    if st != 0:
+        raise SystemExit("device status %d in timed region" % st)
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+
+    # Average duration of the dominant kernel (attention step), CUDA events on
+    # the launching stream around back-to-back launches.
+    n_att = max(10, min(args.steps, 2000))
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(n_att):
+        run_attend()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    attend_s = a0.elapsed_time(a1) / 1e3 / n_att
+    if dist is not None:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    per_step = elapsed / args.steps
+
+    # ---- end to end through the same C ABI with host buffers
+    host = {k: getattr(inp_cpu, k).pin_memory() for k in
+            ("q", "cache", "block_table", "seq_lens", "w_uk", "w_uv")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def e2e_step():
+        for k, t in host.items():
+            getattr(g, k).copy_(t, non_blocking=True)
+        m.plan(g.seq_lens)
+        m.run(g.q, g.cache, g.block_table, g.seq_lens, g.w_uk, g.w_uv, g.scale, out, lse)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    n_e2e = max(3, min(args.e2e_steps, args.steps))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3 / n_e2e
+    if dist is not None:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    hbm, bf16, bf16_sus, peak_src = measured_peaks()
+    gbs = world * stats["cache_bytes"] / per_step / 1e9
+    tflops = world * stats["flops"] / per_step / 1e12
+    attend_gbs = stats["cache_bytes"] / attend_s / 1e9
+    traffic = ncu_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": B, "q_len": T, "heads": H,
+                   "sum_seq_len": stats["sum_len"],
+                   "seq_len": int(inp_cpu.seq_lens[0]) if len(set(inp_cpu.seq_lens.tolist())) == 1
+                   else "varied", "page": 64, "parallelism": "replica x%d" % world,
+                   "l2": "inputs larger than L2 (latent cache %.0f MB > 129 MB L2)" %
+                         (stats["cache_bytes"] / 1e6)},
+        "tflops": tflops, "tokens_per_s": world * stats["tokens"] / per_step,
+        "roofline_step": {"t_roof_us": 1e6 * max(
+            (stats["cache_bytes"] + stats["weight_bytes"]) / (hbm * 1e9),
+            stats["flops"] / (bf16 * 1e12)), "hbm_frac": gbs / world / hbm,
+            "tensor_frac": tflops / world / bf16},
+        "roofline": {"bound": "hbm", "achieved": attend_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": attend_gbs / hbm, "traffic": traffic,
+                     "kernel": "decode_kernel (attend step)", "kernel_us": attend_s * 1e6,
+                     "peak_source": peak_src + " (hbm_gbs, MEASURED_PEAKS.json)"},
+        "e2e": {"value": world * stats["cache_bytes"] / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": args.steps * (1 + binding.lib().mla_decode_kernels_per_run()),
+        "launch_mode": "cuda_graph" if graph_step is not None else "host",
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        dt, nbytes, flops, tokens, text = time_oracle(inp_cpu, budget_s=15.0)
+        line["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s",
+                                "cores": oracle.threads(), "kind": "oracle", "sample": text,
+                                "seconds": dt, "tflops": flops / dt / 1e12}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
