@@ -253,6 +253,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch every step from the host")
+    ap.add_argument("--breakdown", action="store_true",
+                    help="also time each step of the path alone (graph replays)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -384,6 +386,26 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
 
+    breakdown = None
+    if args.breakdown:
+        stages = {"plan": lambda: m.plan(g.seq_lens), "absorb": lambda: m.absorb(g.q, g.w_uk),
+                  "attend": attend_only, "combine": lambda: m.combine(g.scale, lse),
+                  "up_project": lambda: m.up_project(g.w_uv, out)}
+        breakdown = {}
+        for name, fn in stages.items():
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                fn()
+            for _ in range(5):
+                gr.replay()
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            for _ in range(200):
+                gr.replay()
+            b1.record(stream)
+            torch.cuda.synchronize()
+            breakdown[name] = b0.elapsed_time(b1) / 200 * 1e3
+
     if rank != 0:
         dist.destroy_process_group()
         return
@@ -419,6 +441,8 @@ def main():
         "launch_mode": "cuda_graph" if graph_step is not None else "host",
         "clocks": clocks.summary(),
     }
+    if breakdown is not None:
+        line["stage_us"] = breakdown
     if not args.no_cpu_baseline:
         import oracle
         dt, nbytes, flops, tokens, text = time_oracle(inp_cpu, budget_s=15.0)

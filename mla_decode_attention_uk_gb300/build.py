@@ -40,13 +40,13 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps() + [__file__])
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, defines=()) -> str:
     if not force and up_to_date():
         return LIB
     out_dir = os.path.join(HERE, "_build")
     os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if verbose else []
+    extra = (["-Xptxas", "-v"] if verbose else []) + ["-D%s" % d for d in defines]
 
     def compile_one(src):
         obj = os.path.join(out_dir, src.replace(".cu", ".o"))

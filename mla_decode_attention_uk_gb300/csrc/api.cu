@@ -24,7 +24,8 @@ cudaError_t launch_up_project(const CUtensorMap& tm_wuv, const CUtensorMap& tm_o
                               int H, __nv_bfloat16* out, int32_t* status, cudaStream_t st);
 int decode_tiles(int T, int H);
 int decode_q_box_rows(int T, int H);
-cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int grid_ctas,
+cudaError_t decode_max_groups(int T, int H, int sm_count, int* groups);
+cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int groups,
                           const int32_t* block_table, const int32_t* seq_len_eff,
                           const PlanHeader* header, void* ws, const int32_t* seq_first,
                           const int32_t* seq_nsplit, const int32_t* seq_slot,
@@ -103,6 +104,12 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   return r == CUDA_SUCCESS;
 }
 
+int cuda_rc(cudaError_t e) {
+  if (e == cudaSuccess) return MLA_DECODE_OK;
+  cudaGetLastError();
+  return MLA_DECODE_CUDA_ERROR;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_dims(const mla_decode_dims* d) {
@@ -124,12 +131,28 @@ int check_dims(const mla_decode_dims* d) {
   return MLA_DECODE_OK;
 }
 
+// Default number of work ranges = co-resident decode CTA groups (one group =
+// the CTAs covering all query rows of a sequence, a cluster when it has 2 or 4
+// CTAs).  Cached per device and (q_len, heads).
+int g_groups[kMaxDevices][3][9];
+std::mutex g_groups_mu;
+
 int default_ranges(const mla_decode_dims* d, int* R) {
   int sms = 0;
   int rc = sm_count(&sms);
   if (rc) return rc;
-  const int tiles = decode_tiles(d->q_len, d->num_heads);
-  *R = sms / tiles > 0 ? sms / tiles : 1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cuda_rc(cudaErrorUnknown);
+  const int hi = d->num_heads / 16;
+  std::lock_guard<std::mutex> lock(g_groups_mu);
+  int& slot = g_groups[dev][d->q_len][hi];
+  if (slot <= 0) {
+    int groups = 0;
+    if (decode_max_groups(d->q_len, d->num_heads, sms, &groups) != cudaSuccess)
+      return cuda_rc(cudaErrorUnknown);
+    slot = groups;
+  }
+  *R = slot;
   return MLA_DECODE_OK;
 }
 
@@ -147,19 +170,6 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
-int cuda_rc(cudaError_t e) {
-  if (e == cudaSuccess) return MLA_DECODE_OK;
-  cudaGetLastError();
-  return MLA_DECODE_CUDA_ERROR;
-}
-
-int grid_ctas(const mla_decode_dims* d, int* ctas) {
-  int R = 0;
-  int rc = default_ranges(d, &R);
-  if (rc) return rc;
-  *ctas = R * decode_tiles(d->q_len, d->num_heads);
-  return MLA_DECODE_OK;
-}
 
 }  // namespace
 
@@ -268,13 +278,13 @@ int mla_decode_attend(const mla_decode_dims* d, const void* kv_cache, const int3
   if (!make_map(&tm_q, at<void>(ws, L.qlat), rows, kDqk, kDqk, kBoxCols,
                 decode_q_box_rows(d->q_len, d->num_heads), false) ||
       !make_map(&tm_c, kv_cache, static_cast<uint64_t>(d->num_pages) * kPage, kDqk, kDqk,
-                kBoxCols, kPage, true))
+                kBoxCols, 32, true))
     return MLA_DECODE_CUDA_ERROR;
-  int ctas = 0;
-  rc = grid_ctas(d, &ctas);
+  int groups = 0;
+  rc = default_ranges(d, &groups);
   if (rc) return rc;
   return cuda_rc(launch_decode(
-      tm_q, tm_c, ctas, block_table, at<int32_t>(ws, L.seq_len_eff), at<PlanHeader>(ws, L.header),
+      tm_q, tm_c, groups, block_table, at<int32_t>(ws, L.seq_len_eff), at<PlanHeader>(ws, L.header),
       ws, at<int32_t>(ws, L.seq_first), at<int32_t>(ws, L.seq_nsplit), at<int32_t>(ws, L.seq_slot),
       at<__nv_bfloat16>(ws, L.qlo), at<__nv_bfloat16>(ws, L.olat), lse,
       at<int32_t>(ws, L.status), d->batch, d->q_len, d->num_heads, d->max_pages_per_seq,

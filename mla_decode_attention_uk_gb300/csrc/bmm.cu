@@ -29,26 +29,28 @@ namespace mla {
 namespace {
 
 constexpr int kBmmThreads = 128;
-constexpr int kStages = 4;
 constexpr int kABytes = 2 * kBoxBytes;  // 128 m x 64 k, two 64-wide m boxes
 
 enum class BmmMode { kAbsorb, kUpProject };
 
-template <int NT>
+template <int NT, int STAGES>
 struct BmmSmem {
   static constexpr int kBBytes = NT * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTotal = kStages * kStageBytes + 1024;  // + alignment slack
+  static constexpr int kOutBytes = NT * 128 * 2;  // bf16 [NT tokens][128 m] staging tile
+  static constexpr int kPipe = STAGES * kStageBytes;
+  static constexpr int kBody = kPipe > 2 * kOutBytes ? kPipe : 2 * kOutBytes;
+  static constexpr int kTotal = kBody + 1024;  // + alignment slack
 };
 
-template <BmmMode MODE, int NT>
+template <BmmMode MODE, int NT, int STAGES>
 __global__ void __launch_bounds__(kBmmThreads)
 bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
            int BT, int H, int K, int Kx, const __nv_bfloat16* __restrict__ q,
            __nv_bfloat16* __restrict__ out_hi, __nv_bfloat16* __restrict__ out_lo,
            int32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], done_bar;
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], done_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -58,12 +60,13 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   const int h = blockIdx.z;
   const int nk = K / 64;
   constexpr uint32_t kTmemCols = NT < 32 ? 32 : NT;
-  using S = BmmSmem<NT>;
+  using S = BmmSmem<NT, STAGES>;
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const sbase_ptr = smem_raw + (sbase - smem_u32(smem_raw));
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
@@ -85,9 +88,9 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   if (warp == 0) {
     if (elect_one()) {
       for (int kc = 0; kc < nk; ++kc) {
-        const int s = kc % kStages;
-        if (kc >= kStages &&
-            !mbar_wait(smem_u32(&empty_bar[s]), ((kc / kStages) - 1) & 1, &abort_sh, status))
+        const int s = kc % STAGES;
+        if (kc >= STAGES &&
+            !mbar_wait(smem_u32(&empty_bar[s]), ((kc / STAGES) - 1) & 1, &abort_sh, status))
           break;
         const uint32_t a = sbase + s * S::kStageBytes;
         const uint32_t b = a + kABytes;
@@ -101,13 +104,9 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   } else if (warp == 1) {
     if (elect_one()) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, NT, /*a_mn=*/true, /*b_mn=*/false);
-      bool ok = true;
-      for (int kc = 0; kc < nk && ok; ++kc) {
-        const int s = kc % kStages;
-        if (!mbar_wait(smem_u32(&full_bar[s]), (kc / kStages) & 1, &abort_sh, status)) {
-          ok = false;
-          break;
-        }
+      for (int kc = 0; kc < nk; ++kc) {
+        const int s = kc % STAGES;
+        if (!mbar_wait(smem_u32(&full_bar[s]), (kc / STAGES) & 1, &abort_sh, status)) break;
         tc_fence_after();
         const uint32_t a = sbase + s * S::kStageBytes;
         const uint32_t b = a + kABytes;
@@ -124,11 +123,17 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   }
   __syncwarp();
 
-  // Epilogue: thread (warp w, lane i) owns output feature m0 + 32 w + i.
+  // Epilogue.  Thread (warp w, lane i) owns feature m0 + 32 w + i: it moves its
+  // accumulator column (one value per token) into a bf16 [token][128 m] tile in
+  // the now idle pipeline smem, then all threads copy whole 256-byte token rows
+  // to global memory with 16-byte stores.
   const bool have = mbar_wait(smem_u32(&done_bar), 0, &abort_sh, status);
   tc_fence_after();
-  const int m = m0 + warp * 32 + lane;
-  if (have && !abort_sh) {
+  const int ml = warp * 32 + lane;
+  __nv_bfloat16* const tile_hi = reinterpret_cast<__nv_bfloat16*>(sbase_ptr);
+  __nv_bfloat16* const tile_lo = tile_hi + NT * 128;
+  const bool go = have && !abort_sh;
+  if (go) {
 #pragma unroll 1
     for (int c0 = 0; c0 < NT; c0 += 16) {
       uint32_t r[16];
@@ -136,31 +141,38 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
       tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const int tok = tok0 + c0 + j;
-        if (tok >= BT) break;
         const float v = __uint_as_float(r[j]);
-        const size_t row = static_cast<size_t>(tok) * H + h;
-        if constexpr (MODE == BmmMode::kAbsorb) {
-          const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-          out_hi[row * kDqk + m] = hi;
-          out_lo[row * kLora + m] = __float2bfloat16_rn(v - __bfloat162float(hi));
-        } else {
-          out_hi[row * kVHead + m] = __float2bfloat16_rn(v);
-        }
+        const __nv_bfloat16 hv = __float2bfloat16_rn(v);
+        tile_hi[(c0 + j) * 128 + ml] = hv;
+        if constexpr (MODE == BmmMode::kAbsorb)
+          tile_lo[(c0 + j) * 128 + ml] = __float2bfloat16_rn(v - __bfloat162float(hv));
+      }
+    }
+  }
+  __syncthreads();
+  if (go) {
+    const int ntok = min(NT, BT - tok0);
+    // 16 chunks of 16 B per token row; 128 threads cover 8 rows per pass.
+    for (int i = threadIdx.x; i < ntok * 16; i += kBmmThreads) {
+      const int tl = i >> 4, ch = i & 15;
+      const size_t row = static_cast<size_t>(tok0 + tl) * H + h;
+      const uint4 vh = *reinterpret_cast<const uint4*>(tile_hi + tl * 128 + ch * 8);
+      if constexpr (MODE == BmmMode::kAbsorb) {
+        *reinterpret_cast<uint4*>(out_hi + row * kDqk + m0 + ch * 8) = vh;
+        const uint4 vl = *reinterpret_cast<const uint4*>(tile_lo + tl * 128 + ch * 8);
+        *reinterpret_cast<uint4*>(out_lo + row * kLora + m0 + ch * 8) = vl;
+      } else {
+        *reinterpret_cast<uint4*>(out_hi + row * kVHead + m0 + ch * 8) = vh;
       }
     }
     if constexpr (MODE == BmmMode::kAbsorb) {
-      // q_pe passes through unchanged into columns 512..575.
+      // q_pe passes through unchanged into columns 512..575 (8 chunks of 16 B).
       if (blockIdx.y == 0) {
-        for (int i = threadIdx.x; i < NT * (kRope / 2); i += kBmmThreads) {
-          const int tok = tok0 + i / (kRope / 2);
-          const int c = (i % (kRope / 2)) * 2;
-          if (tok < BT) {
-            const size_t row = static_cast<size_t>(tok) * H + h;
-            const uint32_t v =
-                *reinterpret_cast<const uint32_t*>(q + row * kDq + kNope + c);
-            *reinterpret_cast<uint32_t*>(out_hi + row * kDqk + kLora + c) = v;
-          }
+        for (int i = threadIdx.x; i < ntok * 8; i += kBmmThreads) {
+          const int tl = i >> 3, ch = i & 7;
+          const size_t row = static_cast<size_t>(tok0 + tl) * H + h;
+          *reinterpret_cast<uint4*>(out_hi + row * kDqk + kLora + ch * 8) =
+              *reinterpret_cast<const uint4*>(q + row * kDq + kNope + ch * 8);
         }
       }
     }
@@ -177,8 +189,9 @@ template <BmmMode MODE, int NT>
 cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, int H, int K,
                           int Kx, int Mtot, const __nv_bfloat16* q, __nv_bfloat16* hi,
                           __nv_bfloat16* lo, int32_t* status, cudaStream_t st) {
-  auto kern = bmm_kernel<MODE, NT>;
-  const int smem = BmmSmem<NT>::kTotal;
+  constexpr int STAGES = MODE == BmmMode::kAbsorb ? 2 : 4;
+  auto kern = bmm_kernel<MODE, NT, STAGES>;
+  const int smem = BmmSmem<NT, STAGES>::kTotal;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((BT + NT - 1) / NT, Mtot / 128, H);

@@ -10,15 +10,19 @@
 // ranges cut by the planner are merged later by their log-sum-exp.
 //
 // GB300 mapping (one CTA = 64 query rows of one sequence, one work range):
-//   * TMA: the absorbed query tile (9 boxes of 64 x 64 bf16) and each 64-token
-//     page (9 boxes) land in 128B-swizzled shared memory; two page slots.
-//   * QK^T on tcgen05: S[row, key] = sum_576 Q[row] C[key]; M = 128 (rows
-//     64..127 of the MMA are unused), N = 64 keys, fp32 in TMEM, two S buffers.
+//   * Keys stream in 32-token chunks (half a page): the TMA producer gathers a
+//     chunk as 9 boxes of 32 x 64 bf16 (128B swizzle) into a ring of 4-5 slots
+//     of 36 KB, looking the physical page up in the block table.  When the
+//     query rows of a sequence span 2 or 4 CTAs, those CTAs form a cluster and
+//     each loads a share of every chunk with TMA multicast, so a chunk leaves
+//     L2 once per cluster.
+//   * QK^T on tcgen05: S[row, key] = sum_576 Q[row] C[key]; M = 128 (only the
+//     first 64 rows are used), N = 32 keys, fp32 in TMEM, two S buffers.
 //   * Softmax (warps 4-5, one thread per query row, scores read from TMEM):
 //     exp2 with a lazily updated running max (rescale only when the max grows
 //     by more than 2^8), P written to shared memory as bf16.
 //   * PV on tcgen05, transposed: O^T[latent, row] += C^T[latent, key] P^T[key, row]
-//     with the page slot read MN-major as the A operand (M = 128 latent, four
+//     with the chunk slot read MN-major as the A operand (M = 128 latent, four
 //     MMAs for 512) and N = 64 rows; O^T lives in 256 TMEM columns.
 //   * Epilogue (warps 4-7): O / l to bf16 o_lat plus lse for unsplit sequences
 //     (with the first-order correction lse += scale * (q_lo . o) for the bf16
@@ -37,16 +41,15 @@ namespace mla {
 namespace {
 
 constexpr int kDecThreads = 256;
-constexpr int kQBytes = kBoxes * kBoxBytes;     // 72 KB
-constexpr int kPageBytes = kBoxes * kBoxBytes;  // 72 KB
-constexpr int kPTBytes = 64 * 128;              // P^T: 64 rows x 64 keys bf16
-constexpr int kSmemQ = 0;
-constexpr int kSmemSlot0 = kQBytes;
-constexpr int kSmemPT = kQBytes + 2 * kPageBytes;
-constexpr int kDecSmem = kSmemPT + kPTBytes + 1024;  // + alignment slack
+constexpr int kChunk = 32;                         // keys per streamed chunk
+constexpr int kChunkBox = kChunk * 128;            // one 32 x 64 bf16 box: 4 KB
+constexpr int kSlotBytes = kBoxes * kChunkBox;     // 36 KB
+constexpr int kMaxSlots = 6;
+constexpr int kPTBytes = 64 * 128;                 // P^T: 64 rows x (up to 64 keys) bf16
+constexpr int kDynSmemMax = 232448 - 2048;         // opt-in limit minus static smem budget
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 128;                // O^T blocks at 128 + 64 m
-constexpr float kRescaleThreshold = 8.0f;       // log2 units
+constexpr uint32_t kTmemO = 128;                   // O^T blocks at 128 + 64 m
+constexpr float kRescaleThreshold = 8.0f;          // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct DecodeParams {
@@ -65,7 +68,7 @@ struct DecodeParams {
   float* opart;              // [slots, T*H, 512]
   float* lpart;              // [slots, T*H]
   int32_t* status;
-  int B, T, H, max_pages, num_pages, tiles, q_box_rows;
+  int B, T, H, max_pages, num_pages, tiles, q_box_rows, num_slots, cluster;
   float scale, scale_log2;
 };
 
@@ -87,7 +90,6 @@ struct PieceWalker {
   int b, p, b1, p1;
   __device__ PieceWalker(const DecodeParams& P, int k)
       : b(P.range_b[k]), p(P.range_p[k]), b1(P.range_b[k + 1]), p1(P.range_p[k + 1]) {}
-  // Next piece: returns false when the range is exhausted.
   __device__ bool next(const DecodeParams& P, int& pb, int& pbeg, int& pend) {
     while (b < b1 || (b == b1 && p < p1)) {
       const int pages = (P.seq_len_eff[b] + kPage - 1) / kPage;
@@ -106,12 +108,26 @@ struct PieceWalker {
   }
 };
 
+// Chunks of a piece: two per page, except a last page whose keys all fall in
+// its first half.  Chunk i of the piece covers keys key0(i) .. key0(i) + 31.
+struct ChunkRange {
+  int pbeg, nchunks;
+  __device__ ChunkRange(int L, int pb, int pe) : pbeg(pb) {
+    nchunks = 2 * (pe - pb);
+    const int last_page = (L - 1) / kPage;
+    if (pe - 1 == last_page && L - last_page * kPage <= kChunk) nchunks -= 1;
+  }
+  __device__ int page(int i) const { return pbeg + (i >> 1); }
+  __device__ int half(int i) const { return i & 1; }
+  __device__ int key0(int i) const { return pbeg * kPage + i * kChunk; }
+};
+
 __global__ void __launch_bounds__(kDecThreads, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
               DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t q_full, q_free, slot_full[2], slot_empty[2], s_full[2],
-      s_free[2], p_full, p_free, o_full, o_free, drain_bar;
+  __shared__ __align__(8) uint64_t q_full, q_free, slot_full[kMaxSlots], slot_empty[kMaxSlots],
+      s_full[2], s_free[2], p_full, p_free, o_full, o_free, drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ float alpha_sh[64];
@@ -124,6 +140,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int G = gridDim.x / P.tiles;
   const int R = P.header->num_ranges;
   const int TH = P.T * P.H;
+  const int NS = P.num_slots;
+  const int CS = P.cluster;                       // CTAs sharing each chunk (1, 2 or 4)
+  const int crank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const uint16_t cmask = static_cast<uint16_t>((1u << CS) - 1u);
   {
     const WsLayout L = make_layout(P.B, P.T, P.H, R);
     P.range_b = reinterpret_cast<const int32_t*>(P.ws + L.range_b);
@@ -131,15 +151,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     P.lpart = reinterpret_cast<float*>(P.ws + L.lpart);
     P.opart = reinterpret_cast<float*>(P.ws + L.opart);
   }
+  const uint32_t q_box_bytes = static_cast<uint32_t>(P.q_box_rows) * 128u;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sQ = sbase + kSmemQ, sSlot0 = sbase + kSmemSlot0, sPT = sbase + kSmemPT;
+  const uint32_t sQ = sbase;
+  const uint32_t sSlot0 = sQ + kBoxes * q_box_bytes;
+  const uint32_t sPT = sSlot0 + NS * kSlotBytes;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&q_full), 1);
     mbar_init(smem_u32(&q_free), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&slot_full[i]), 1);
-      mbar_init(smem_u32(&slot_empty[i]), 1);
+      mbar_init(smem_u32(&slot_empty[i]), CS);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
       mbar_init(smem_u32(&s_free[i]), 2);
     }
@@ -159,14 +184,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   }
   tc_fence_before();
   __syncthreads();
+  // Peers multicast into this CTA's slots and arrive on its barriers: they
+  // must all be initialised first.
+  if (CS > 1) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (elect_one()) {
-      const uint64_t pol_stream = l2_policy_evict_first();
-      const uint32_t q_bytes = static_cast<uint32_t>(P.q_box_rows) * 128u * kBoxes;
+      const uint32_t q_bytes = q_box_bytes * kBoxes;
       int g = 0, pc = 0;
       bool ok = true;
       for (int k = k0; k < R && ok; k += G) {
@@ -180,24 +207,33 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           const int qrow = b * TH + tile * kTileRows;
           mbar_expect_tx(smem_u32(&q_full), q_bytes);
           for (int j = 0; j < kBoxes; ++j)
-            tma_load_2d(sQ + j * kBoxBytes, &tm_q, j * kBoxCols, qrow, smem_u32(&q_full));
-          for (int p = pb; p < pe; ++p, ++g) {
-            const int s = g & 1;
-            if (g >= 2 &&
-                !mbar_wait(smem_u32(&slot_empty[s]), ((g >> 1) - 1) & 1, &abort_sh, P.status)) {
+            tma_load_2d(sQ + j * q_box_bytes, &tm_q, j * kBoxCols, qrow, smem_u32(&q_full));
+          const ChunkRange cr(P.seq_len_eff[b], pb, pe);
+          int pg = 0;
+          for (int i = 0; i < cr.nchunks; ++i, ++g) {
+            const int s = g % NS, u = g / NS;
+            if (u > 0 && !mbar_wait(smem_u32(&slot_empty[s]), (u - 1) & 1, &abort_sh, P.status)) {
               ok = false;
               break;
             }
-            int pg = __ldg(P.block_table + static_cast<size_t>(b) * P.max_pages + p);
-            if (pg < 0 || pg >= P.num_pages) {
-              atomicCAS(P.status, 0, MLA_STATUS_BOUNDS);
-              pg = 0;
+            if (cr.half(i) == 0 || i == 0) {
+              pg = __ldg(P.block_table + static_cast<size_t>(b) * P.max_pages + cr.page(i));
+              if (pg < 0 || pg >= P.num_pages) {
+                atomicCAS(P.status, 0, MLA_STATUS_BOUNDS);
+                pg = 0;
+              }
             }
-            const uint32_t dst = sSlot0 + s * kPageBytes;
-            mbar_expect_tx(smem_u32(&slot_full[s]), kPageBytes);
-            for (int j = 0; j < kBoxes; ++j)
-              tma_load_2d_hint(dst + j * kBoxBytes, &tm_c, j * kBoxCols, pg * kPage,
-                               smem_u32(&slot_full[s]), pol_stream);
+            const uint32_t dst = sSlot0 + s * kSlotBytes;
+            const uint32_t fb = smem_u32(&slot_full[s]);
+            const int row = pg * kPage + cr.half(i) * kChunk;
+            mbar_expect_tx(fb, kSlotBytes);
+            if (CS == 1) {
+              for (int j = 0; j < kBoxes; ++j)
+                tma_load_2d(dst + j * kChunkBox, &tm_c, j * kBoxCols, row, fb);
+            } else {
+              for (int j = crank; j < kBoxes; j += CS)
+                tma_load_2d_mc(dst + j * kChunkBox, &tm_c, j * kBoxCols, row, fb, cmask);
+            }
           }
           ++pc;
         }
@@ -206,7 +242,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kChunk, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 64, true, false);
       int g = 0, pc = 0;
       bool ok = true;
@@ -215,18 +251,23 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (first && pc > 0 && !mbar_wait(smem_u32(&o_free), (pc - 1) & 1, &abort_sh, P.status))
           return false;
         tc_fence_after();
-        const uint32_t slot = sSlot0 + (gg & 1) * kPageBytes;
+        const int s = gg % NS;
+        const uint32_t slot = sSlot0 + s * kSlotBytes;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sdesc_sw128(slot + (2 * m) * kBoxBytes + kk * 2048, kBoxBytes, 1024);
+          for (int kk = 0; kk < kChunk / 16; ++kk) {
+            const uint64_t ad =
+                sdesc_sw128(slot + (2 * m) * kChunkBox + kk * 2048, kChunkBox, 1024);
             const uint64_t bd = sdesc_sw128(sPT + kk * 32, 16, 1024);
             umma_bf16(tmem + kTmemO + 64 * m, ad, bd, idesc_pv, !(first && kk == 0));
           }
         }
         umma_commit(smem_u32(&p_free));
-        umma_commit(smem_u32(&slot_empty[gg & 1]));
+        if (CS == 1)
+          umma_commit(smem_u32(&slot_empty[s]));
+        else
+          umma_commit_mc(smem_u32(&slot_empty[s]), cmask);
         return true;
       };
       for (int k = k0; k < R && ok; k += G) {
@@ -237,35 +278,36 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ok = false;
             break;
           }
-          const int np = pe - pb;
-          for (int i = 0; i < np; ++i, ++g) {
-            const int s = g & 1;
-            if (!mbar_wait(smem_u32(&slot_full[s]), (g >> 1) & 1, &abort_sh, P.status) ||
+          const ChunkRange cr(P.seq_len_eff[b], pb, pe);
+          const int nc = cr.nchunks;
+          for (int i = 0; i < nc; ++i, ++g) {
+            const int s = g % NS, sb = g & 1;
+            if (!mbar_wait(smem_u32(&slot_full[s]), (g / NS) & 1, &abort_sh, P.status) ||
                 (g >= 2 &&
-                 !mbar_wait(smem_u32(&s_free[s]), ((g >> 1) - 1) & 1, &abort_sh, P.status))) {
+                 !mbar_wait(smem_u32(&s_free[sb]), ((g >> 1) - 1) & 1, &abort_sh, P.status))) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t slot = sSlot0 + s * kPageBytes;
+            const uint32_t slot = sSlot0 + s * kSlotBytes;
 #pragma unroll
             for (int j = 0; j < kBoxes; ++j) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = sdesc_sw128(sQ + j * kBoxBytes + kk * 32, 16, 1024);
-                const uint64_t bd = sdesc_sw128(slot + j * kBoxBytes + kk * 32, 16, 1024);
-                umma_bf16(tmem + 64 * s, ad, bd, idesc_qk, (j | kk) != 0);
+                const uint64_t ad = sdesc_sw128(sQ + j * q_box_bytes + kk * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(slot + j * kChunkBox + kk * 32, 16, 1024);
+                umma_bf16(tmem + kChunk * sb, ad, bd, idesc_qk, (j | kk) != 0);
               }
             }
-            umma_commit(smem_u32(&s_full[s]));
-            if (i == np - 1) umma_commit(smem_u32(&q_free));
+            umma_commit(smem_u32(&s_full[sb]));
+            if (i == nc - 1) umma_commit(smem_u32(&q_free));
             if (i > 0 && !issue_pv(g - 1, i - 1 == 0)) {
               ok = false;
               break;
             }
           }
           if (!ok) break;
-          if (!issue_pv(g - 1, np == 1)) {
+          if (!issue_pv(g - 1, nc == 1)) {
             ok = false;
             break;
           }
@@ -294,30 +336,30 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int L = P.seq_len_eff[b];
         const int n_row = row_ok ? L - P.T + r / P.H + 1 : 0;
         float m_used = -INFINITY, l = 0.0f;
-        const int np = pe - pb;
-        for (int i = 0; i < np; ++i, ++g) {
-          const int s = g & 1;
+        const ChunkRange cr(L, pb, pe);
+        const int nc = cr.nchunks;
+        for (int i = 0; i < nc; ++i, ++g) {
+          const int sb = g & 1;
           bool need = false;
           bool bad = false;
           if (srow) {
-            if (!mbar_wait(smem_u32(&s_full[s]), (g >> 1) & 1, &abort_sh, P.status)) bad = true;
+            if (!mbar_wait(smem_u32(&s_full[sb]), (g >> 1) & 1, &abort_sh, P.status)) bad = true;
             bad = __any_sync(0xffffffffu, bad);  // tcgen05.ld below is warp-collective
-            uint32_t v[64];
+            uint32_t v[kChunk];
             if (!bad) {
               tc_fence_after();
-              tmem_ld_x32(tmem + lane_off + 64 * s, v);
-              tmem_ld_x32(tmem + lane_off + 64 * s + 32, v + 32);
+              tmem_ld_x32(tmem + lane_off + kChunk * sb, v);
               tmem_wait_ld();
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s_free[s]));
+            if (lane == 0) mbar_arrive(smem_u32(&s_free[sb]));
             if (!bad) {
-              const int key0 = (pb + i) * kPage;
-              float x[64];
+              const int key0 = cr.key0(i);
+              float x[kChunk];
               float pmax = -INFINITY;
 #pragma unroll
-              for (int j = 0; j < 64; ++j) {
+              for (int j = 0; j < kChunk; ++j) {
                 x[j] = (key0 + j < n_row) ? __uint_as_float(v[j]) * P.scale_log2 : -INFINITY;
                 pmax = fmaxf(pmax, x[j]);
               }
@@ -327,10 +369,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 m_used = pmax;
                 need = i > 0;
               }
-              uint32_t packed[32];
+              uint32_t packed[kChunk / 2];
               float sum = 0.0f;
 #pragma unroll
-              for (int j = 0; j < 64; j += 2) {
+              for (int j = 0; j < kChunk; j += 2) {
                 const float p0 = (x[j] == -INFINITY) ? 0.0f : ex2_approx(x[j] - m_used);
                 const float p1 = (x[j + 1] == -INFINITY) ? 0.0f : ex2_approx(x[j + 1] - m_used);
                 sum += p0 + p1;
@@ -338,13 +380,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               }
               l = l * alpha + sum;
               alpha_sh[c] = alpha;
-              // The P^T buffer is free once the previous page's PV has finished.
+              // The P^T buffer is free once the previous chunk's PV has finished.
               if (g >= 1 && !mbar_wait(smem_u32(&p_free), (g - 1) & 1, &abort_sh, P.status))
                 bad = true;
               if (!bad) {
                 const uint32_t rowaddr = sPT + c * 128;
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
+                for (int q = 0; q < kChunk / 8; ++q)
                   st_shared_v4(rowaddr + ((q ^ (c & 7)) << 4), packed[4 * q], packed[4 * q + 1],
                                packed[4 * q + 2], packed[4 * q + 3]);
                 fence_proxy_async_smem();
@@ -371,7 +413,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             tmem_wait_st();
             tc_fence_before();
-            named_bar_sync(1, 128);  // alpha_sh is rewritten by the next page
+            named_bar_sync(1, 128);  // alpha_sh is rewritten by the next chunk
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&p_full));
@@ -392,6 +434,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const size_t part_base =
             nsplit > 1 ? (static_cast<size_t>(P.seq_slot[b] + split) * TH + tile * kTileRows) : 0;
         const int rows_here = min(kTileRows, TH - tile * kTileRows);
+        const __nv_bfloat16* __restrict__ qlo = P.qlo;
+        __nv_bfloat16* __restrict__ olat = P.olat;
+        float* __restrict__ opart = P.opart;
 #pragma unroll 1
         for (int h2 = 0; h2 < 2; ++h2) {
           float corr[32];
@@ -399,21 +444,31 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           for (int j = 0; j < 32; ++j) corr[j] = 0.0f;
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) {
+            const int lat = 128 * m + 32 * wq + lane;
+            // Issue this block's q_lo loads before any store so they overlap.
+            float lo[32];
+            if (nsplit <= 1) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const int cc = 32 * h2 + j;
+                lo[j] = cc < rows_here
+                            ? __bfloat162float(qlo[(row_base + cc) * kLora + lat])
+                            : 0.0f;
+              }
+            }
             uint32_t v[32];
             tmem_ld_x32(tmem + lane_off + kTmemO + 64 * m + 32 * h2, v);
             tmem_wait_ld();
-            const int lat = 128 * m + 32 * wq + lane;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int cc = 32 * h2 + j;
               if (cc < rows_here) {
                 const float val = __uint_as_float(v[j]) * inv_l_sh[cc];
                 if (nsplit > 1) {
-                  P.opart[(part_base + cc) * kLora + lat] = val;
+                  opart[(part_base + cc) * kLora + lat] = val;
                 } else {
-                  const size_t o = (row_base + cc) * kLora + lat;
-                  P.olat[o] = __float2bfloat16_rn(val);
-                  corr[j] += __bfloat162float(P.qlo[o]) * val;
+                  olat[(row_base + cc) * kLora + lat] = __float2bfloat16_rn(val);
+                  corr[j] += lo[j] * val;
                 }
               }
             }
@@ -449,6 +504,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
+  // No peer may still arrive on this CTA's barriers once it exits.
+  if (CS > 1) cluster_sync_all();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -462,16 +519,61 @@ int decode_q_box_rows(int T, int H) {
   const int r = T * H;
   return r >= kTileRows ? kTileRows : ((r + 7) / 8) * 8;
 }
+int decode_num_slots(int T, int H) {
+  const int q_bytes = kBoxes * decode_q_box_rows(T, H) * 128;
+  int ns = (kDynSmemMax - 1024 - q_bytes - kPTBytes) / kSlotBytes;
+  return ns > kMaxSlots ? kMaxSlots : ns;
+}
+int decode_smem_bytes(int T, int H) {
+  return 1024 + kBoxes * decode_q_box_rows(T, H) * 128 + decode_num_slots(T, H) * kSlotBytes +
+         kPTBytes;
+}
+// CTAs that share each key chunk through TMA multicast (a cluster).
+int decode_cluster_size(int T, int H) {
+  const int tiles = decode_tiles(T, H);
+  return (tiles == 2 || tiles == 4) ? tiles : 1;
+}
 
-cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int grid_ctas,
+// Largest number of co-resident CTA groups (clusters of decode_cluster_size).
+cudaError_t decode_max_groups(int T, int H, int sm_count, int* groups) {
+  const int cs = decode_cluster_size(T, H);
+  const int tiles = decode_tiles(T, H);
+  const int smem = decode_smem_bytes(T, H);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem);
+  if (e != cudaSuccess) return e;
+  if (cs == 1) {
+    *groups = sm_count / tiles > 0 ? sm_count / tiles : 1;
+    return cudaSuccess;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs * (sm_count / cs), 1, 1);
+  cfg.blockDim = dim3(kDecThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, decode_kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  *groups = n > 0 ? n : 1;
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int groups,
                           const int32_t* block_table, const int32_t* seq_len_eff,
                           const PlanHeader* header, void* ws, const int32_t* seq_first,
                           const int32_t* seq_nsplit, const int32_t* seq_slot,
                           const __nv_bfloat16* qlo, __nv_bfloat16* olat, float* lse,
                           int32_t* status, int B, int T, int H, int max_pages,
                           int num_pages, float scale, cudaStream_t st) {
+  const int smem = decode_smem_bytes(T, H);
   cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kDecSmem);
+                                       smem);
   if (e != cudaSuccess) return e;
   DecodeParams P;
   P.block_table = block_table;
@@ -496,9 +598,25 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
   P.num_pages = num_pages;
   P.tiles = decode_tiles(T, H);
   P.q_box_rows = decode_q_box_rows(T, H);
+  P.num_slots = decode_num_slots(T, H);
+  P.cluster = decode_cluster_size(T, H);
   P.scale = scale;
   P.scale_log2 = scale * 1.4426950408889634f;
-  decode_kernel<<<grid_ctas, kDecThreads, kDecSmem, st>>>(tm_q, tm_c, P);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(groups * P.tiles, 1, 1);
+  cfg.blockDim = dim3(kDecThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = P.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = P.cluster > 1 ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, decode_kernel, tm_q, tm_c, P);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -32,7 +32,10 @@ def test_absorb_bmm_matches_fp32_matmul():
     ref = torch.einsum("bthk,hkl->bthl", inp.q[..., :128].double(), inp.w_uk.double())
     ref = ref.reshape(-1, 512)
     got = hi[:, :512].double() + lo.double()
-    assert (got - ref).abs().max().item() < 2e-5
+    # hi + lo carries ~16 significant bits: the bf16 rounding of the residual
+    # is at most 2^-9 of a residual that is itself at most 2^-9 of the value;
+    # fp32 accumulation over K = 128 adds far less.
+    assert ((got - ref).abs() <= ref.abs() * 2.0 ** -16 + 2e-6).all()
     assert torch.equal(hi[:, 512:], inp.q[..., 128:].reshape(-1, 64).float())
     # hi is the bf16 rounding of the fp32 product, lo the bf16 rounding of the rest
     assert (hi[:, :512].double() - ref).abs().max().item() <= ref.abs().max().item() * 2 ** -8
