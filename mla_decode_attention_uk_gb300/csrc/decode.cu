@@ -127,7 +127,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, q_free, slot_full[kMaxSlots], slot_empty[kMaxSlots],
-      s_full[2], s_free[2], p_full, p_free, o_full, o_free, drain_bar;
+      s_full[2], s_free[2], p_full[2], p_free[2], o_full, o_free, drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ float alpha_sh[64];
@@ -168,8 +168,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(smem_u32(&s_full[i]), 1);
       mbar_init(smem_u32(&s_free[i]), 2);
     }
-    mbar_init(smem_u32(&p_full), 4);
-    mbar_init(smem_u32(&p_free), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&p_full[i]), 4);
+      mbar_init(smem_u32(&p_free[i]), 1);
+    }
     mbar_init(smem_u32(&o_full), 1);
     mbar_init(smem_u32(&o_free), 4);
     mbar_init(smem_u32(&drain_bar), 1);
@@ -247,7 +249,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       int g = 0, pc = 0;
       bool ok = true;
       auto issue_pv = [&](int gg, bool first) -> bool {
-        if (!mbar_wait(smem_u32(&p_full), gg & 1, &abort_sh, P.status)) return false;
+        const int pb2 = gg & 1;  // P^T half used by this chunk
+        if (!mbar_wait(smem_u32(&p_full[pb2]), (gg >> 1) & 1, &abort_sh, P.status)) return false;
         if (first && pc > 0 && !mbar_wait(smem_u32(&o_free), (pc - 1) & 1, &abort_sh, P.status))
           return false;
         tc_fence_after();
@@ -259,11 +262,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           for (int kk = 0; kk < kChunk / 16; ++kk) {
             const uint64_t ad =
                 sdesc_sw128(slot + (2 * m) * kChunkBox + kk * 2048, kChunkBox, 1024);
-            const uint64_t bd = sdesc_sw128(sPT + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sPT + (2 * pb2 + kk) * 32, 16, 1024);
             umma_bf16(tmem + kTmemO + 64 * m, ad, bd, idesc_pv, !(first && kk == 0));
           }
         }
-        umma_commit(smem_u32(&p_free));
+        umma_commit(smem_u32(&p_free[pb2]));
         if (CS == 1)
           umma_commit(smem_u32(&slot_empty[s]));
         else
@@ -380,22 +383,33 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               }
               l = l * alpha + sum;
               alpha_sh[c] = alpha;
-              // The P^T buffer is free once the previous chunk's PV has finished.
-              if (g >= 1 && !mbar_wait(smem_u32(&p_free), (g - 1) & 1, &abort_sh, P.status))
+              // P^T is double-buffered in the two 64-byte halves of each
+              // 128-byte swizzled row; this half is free once the PV of the
+              // chunk before last has finished.
+              const int pb2 = g & 1;
+              if (g >= 2 && !mbar_wait(smem_u32(&p_free[pb2]), ((g >> 1) - 1) & 1, &abort_sh,
+                                       P.status))
                 bad = true;
               if (!bad) {
                 const uint32_t rowaddr = sPT + c * 128;
 #pragma unroll
                 for (int q = 0; q < kChunk / 8; ++q)
-                  st_shared_v4(rowaddr + ((q ^ (c & 7)) << 4), packed[4 * q], packed[4 * q + 1],
-                               packed[4 * q + 2], packed[4 * q + 3]);
+                  st_shared_v4(rowaddr + (((4 * pb2 + q) ^ (c & 7)) << 4), packed[4 * q],
+                               packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
                 fence_proxy_async_smem();
               }
             }
           }
-          if (bar_any(1, 128, bad)) { fail = true; break; }
-          if (bar_any(1, 128, need)) {
-            // Some row's running max moved: rescale its O^T column (all 4 quarters).
+          // One barrier per chunk: a timeout anywhere or a rescale request.
+          if (bar_any(1, 128, bad || need)) {
+            // Some row's running max moved: rescale its O^T column (all 4
+            // quarters) once the previous chunk's PV has landed.
+            bool f = *static_cast<volatile int*>(&abort_sh) != 0;
+            if (!f && g >= 1 &&
+                !mbar_wait(smem_u32(&p_free[(g - 1) & 1]), ((g - 1) >> 1) & 1, &abort_sh,
+                           P.status))
+              f = true;
+            if (bar_any(1, 128, f)) { fail = true; break; }
             tc_fence_after();
 #pragma unroll 1
             for (int m = 0; m < 4; ++m) {
@@ -416,7 +430,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             named_bar_sync(1, 128);  // alpha_sh is rewritten by the next chunk
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&p_full));
+          if (lane == 0) mbar_arrive(smem_u32(&p_full[g & 1]));
         }
         if (fail) break;
 
