@@ -16,11 +16,12 @@
 //     query rows of a sequence span 2 or 4 CTAs, those CTAs form a cluster and
 //     each loads a share of every chunk with TMA multicast, so a chunk leaves
 //     L2 once per cluster.
-//   * QK^T on tcgen05: S[row, key] = sum_576 Q[row] C[key]; M = 128 (only the
-//     first 64 rows are used), N = 32 keys, fp32 in TMEM, two S buffers.
-//   * Softmax (warps 4-5, one thread per query row, scores read from TMEM):
-//     exp2 with a lazily updated running max (rescale only when the max grows
-//     by more than 2^8), P written to shared memory as bf16.
+//   * QK^T on tcgen05: S[row, key] = sum_576 Q[row] C[key]; M = 64 rows, N = 32
+//     keys, fp32 in TMEM (an M = 64 accumulator puts 16 rows in each 32-lane
+//     quarter), two S buffers.
+//   * Softmax (warps 4-7, 16 rows each, two threads per row holding the even
+//     and odd keys): exp2 with a lazily updated running max (rescale only
+//     when the max grows by more than 2^8), P written to shared memory as bf16.
 //   * PV on tcgen05, transposed: O^T[latent, row] += C^T[latent, key] P^T[key, row]
 //     with the chunk slot read MN-major as the A operand (M = 128 latent, four
 //     MMAs for 512) and N = 64 rows; O^T lives in 256 TMEM columns.
@@ -28,7 +29,8 @@
 //     (with the first-order correction lse += scale * (q_lo . o) for the bf16
 //     rounding of the absorbed query), or fp32 partials for split ones.
 // Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 3 idle, 4-7 softmax
-// and epilogue.
+// and epilogue.  The MMA issuer works from precomputed descriptors so one
+// instruction costs an add and the issue itself.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -166,7 +168,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
-      mbar_init(smem_u32(&s_free[i]), 2);
+      mbar_init(smem_u32(&s_free[i]), 4);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&p_full[i]), 4);
@@ -244,8 +246,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kChunk, false, false);
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(64, kChunk, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 64, true, false);
+      // Descriptors differ only in the start-address field (bits 0-13, in
+      // 16-byte units), so each MMA adds a small constant to a base.
+      const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dslot0 = sdesc_sw128(sSlot0, 16, 1024);
+      const uint64_t dpv0 = sdesc_sw128(sSlot0, kChunkBox, 1024);
+      const uint64_t dpt0 = sdesc_sw128(sPT, 16, 1024);
+      const uint32_t qbox16 = q_box_bytes >> 4;
       int g = 0, pc = 0;
       bool ok = true;
       auto issue_pv = [&](int gg, bool first) -> bool {
@@ -255,15 +264,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           return false;
         tc_fence_after();
         const int s = gg % NS;
-        const uint32_t slot = sSlot0 + s * kSlotBytes;
+        const uint64_t ad0 = dpv0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
+        const uint64_t bd0 = dpt0 + static_cast<uint64_t>(pb2 * 4);
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
 #pragma unroll
           for (int kk = 0; kk < kChunk / 16; ++kk) {
-            const uint64_t ad =
-                sdesc_sw128(slot + (2 * m) * kChunkBox + kk * 2048, kChunkBox, 1024);
-            const uint64_t bd = sdesc_sw128(sPT + (2 * pb2 + kk) * 32, 16, 1024);
-            umma_bf16(tmem + kTmemO + 64 * m, ad, bd, idesc_pv, !(first && kk == 0));
+            umma_bf16(tmem + kTmemO + 64 * m, ad0 + ((2 * m * kChunkBox + kk * 2048) >> 4),
+                      bd0 + kk * 2, idesc_pv, !(first && kk == 0));
           }
         }
         umma_commit(smem_u32(&p_free[pb2]));
@@ -292,14 +300,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               break;
             }
             tc_fence_after();
-            const uint32_t slot = sSlot0 + s * kSlotBytes;
+            const uint64_t bd0 = dslot0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
 #pragma unroll
             for (int j = 0; j < kBoxes; ++j) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = sdesc_sw128(sQ + j * q_box_bytes + kk * 32, 16, 1024);
-                const uint64_t bd = sdesc_sw128(slot + j * kChunkBox + kk * 32, 16, 1024);
-                umma_bf16(tmem + kChunk * sb, ad, bd, idesc_qk, (j | kk) != 0);
+                umma_bf16(tmem + kChunk * sb, dq0 + (j * qbox16 + kk * 2),
+                          bd0 + ((j * kChunkBox) >> 4) + kk * 2, idesc_qk, (j | kk) != 0);
               }
             }
             umma_commit(smem_u32(&s_full[sb]));
@@ -325,79 +332,90 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
     const int wq = warp - 4;                    // TMEM lane quarter
-    const int c = wq * 32 + lane;               // query row in tile (valid for wq < 2)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const bool srow = wq < 2;
+    // Softmax ownership (M = 64 accumulator, 16x64b loads): this thread holds
+    // row `srow_c` of the tile, keys of parity `par`; par 0 writes row results.
+    const int rig = (lane >> 2) + 8 * (lane & 1);
+    const int par = (lane >> 1) & 1;
+    const int srow_c = 16 * wq + rig;
+    const bool owner = par == 0;
     int g = 0, pc = 0;
     bool fail = false;
     for (int k = k0; k < R && !fail; k += G) {
       PieceWalker w(P, k);
       int b, pb, pe;
       while (!fail && w.next(P, b, pb, pe)) {
-        const int r = tile * kTileRows + c;     // row within the sequence's T*H rows
-        const bool row_ok = srow && r < TH;
+        const int r = tile * kTileRows + srow_c;  // row within the sequence's T*H rows
+        const bool row_ok = r < TH;
         const int L = P.seq_len_eff[b];
         const int n_row = row_ok ? L - P.T + r / P.H + 1 : 0;
-        float m_used = -INFINITY, l = 0.0f;
+        float m_used = -INFINITY, l = 0.0f;     // l: this thread's half of the row sum
         const ChunkRange cr(L, pb, pe);
         const int nc = cr.nchunks;
         for (int i = 0; i < nc; ++i, ++g) {
           const int sb = g & 1;
           bool need = false;
-          bool bad = false;
-          if (srow) {
-            if (!mbar_wait(smem_u32(&s_full[sb]), (g >> 1) & 1, &abort_sh, P.status)) bad = true;
-            bad = __any_sync(0xffffffffu, bad);  // tcgen05.ld below is warp-collective
-            uint32_t v[kChunk];
-            if (!bad) {
-              tc_fence_after();
-              tmem_ld_x32(tmem + lane_off + kChunk * sb, v);
-              tmem_wait_ld();
+          bool bad = !mbar_wait(smem_u32(&s_full[sb]), (g >> 1) & 1, &abort_sh, P.status);
+          bad = __any_sync(0xffffffffu, bad);  // tcgen05.ld below is warp-collective
+          uint32_t v[kChunk / 2];
+          if (!bad) {
+            tc_fence_after();
+            tmem_ld_16x64b_x16(tmem + lane_off + kChunk * sb, v);
+            tmem_wait_ld();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&s_free[sb]));
+          if (!bad) {
+            const int kb = cr.key0(i) + par;    // key of v[0]; v[j] is key kb + 2 j
+            float x[kChunk / 2];
+            float pmax = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kChunk / 2; ++j) {
+              x[j] = (kb + 2 * j < n_row) ? __uint_as_float(v[j]) * P.scale_log2 : -INFINITY;
+              pmax = fmaxf(pmax, x[j]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s_free[sb]));
+            pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 2));
+            float alpha = 1.0f;
+            if (pmax > m_used + kRescaleThreshold) {
+              alpha = (m_used == -INFINITY) ? 0.0f : ex2_approx(m_used - pmax);
+              m_used = pmax;
+              need = i > 0;
+            }
+            float p[kChunk / 2];
+            float sum = 0.0f;
+#pragma unroll
+            for (int j = 0; j < kChunk / 2; ++j) {
+              p[j] = (x[j] == -INFINITY) ? 0.0f : ex2_approx(x[j] - m_used);
+              sum += p[j];
+            }
+            l = l * alpha + sum;
+            if (owner) alpha_sh[srow_c] = alpha;
+            // Pair up neighbouring keys: the even-key thread writes keys 0..15
+            // of the chunk, the odd-key thread keys 16..31.
+            uint32_t packed[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float send = par ? p[q] : p[8 + q];
+              const float recv = __shfl_xor_sync(0xffffffffu, send, 2);
+              packed[q] = par ? pack_bf16x2(recv, p[8 + q]) : pack_bf16x2(p[q], recv);
+            }
+            // P^T is double-buffered in the two 64-byte halves of each
+            // 128-byte swizzled row; this half is free once the PV of the
+            // chunk before last has finished.
+            const int pb2 = g & 1;
+            if (g >= 2 && !mbar_wait(smem_u32(&p_free[pb2]), ((g >> 1) - 1) & 1, &abort_sh,
+                                     P.status))
+              bad = true;
             if (!bad) {
-              const int key0 = cr.key0(i);
-              float x[kChunk];
-              float pmax = -INFINITY;
+              const uint32_t rowaddr = sPT + srow_c * 128;
 #pragma unroll
-              for (int j = 0; j < kChunk; ++j) {
-                x[j] = (key0 + j < n_row) ? __uint_as_float(v[j]) * P.scale_log2 : -INFINITY;
-                pmax = fmaxf(pmax, x[j]);
+              for (int q = 0; q < 2; ++q) {
+                const int lchunk = 4 * pb2 + 2 * par + q;
+                st_shared_v4(rowaddr + ((lchunk ^ (srow_c & 7)) << 4), packed[4 * q],
+                             packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
               }
-              float alpha = 1.0f;
-              if (pmax > m_used + kRescaleThreshold) {
-                alpha = (m_used == -INFINITY) ? 0.0f : ex2_approx(m_used - pmax);
-                m_used = pmax;
-                need = i > 0;
-              }
-              uint32_t packed[kChunk / 2];
-              float sum = 0.0f;
-#pragma unroll
-              for (int j = 0; j < kChunk; j += 2) {
-                const float p0 = (x[j] == -INFINITY) ? 0.0f : ex2_approx(x[j] - m_used);
-                const float p1 = (x[j + 1] == -INFINITY) ? 0.0f : ex2_approx(x[j + 1] - m_used);
-                sum += p0 + p1;
-                packed[j / 2] = pack_bf16x2(p0, p1);
-              }
-              l = l * alpha + sum;
-              alpha_sh[c] = alpha;
-              // P^T is double-buffered in the two 64-byte halves of each
-              // 128-byte swizzled row; this half is free once the PV of the
-              // chunk before last has finished.
-              const int pb2 = g & 1;
-              if (g >= 2 && !mbar_wait(smem_u32(&p_free[pb2]), ((g >> 1) - 1) & 1, &abort_sh,
-                                       P.status))
-                bad = true;
-              if (!bad) {
-                const uint32_t rowaddr = sPT + c * 128;
-#pragma unroll
-                for (int q = 0; q < kChunk / 8; ++q)
-                  st_shared_v4(rowaddr + (((4 * pb2 + q) ^ (c & 7)) << 4), packed[4 * q],
-                               packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-                fence_proxy_async_smem();
-              }
+              fence_proxy_async_smem();
             }
           }
           // One barrier per chunk: a timeout anywhere or a rescale request.
@@ -415,14 +433,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             for (int m = 0; m < 4; ++m) {
 #pragma unroll 1
               for (int h2 = 0; h2 < 2; ++h2) {
-                uint32_t v[32];
+                uint32_t vv[32];
                 const uint32_t ta = tmem + lane_off + kTmemO + 64 * m + 32 * h2;
-                tmem_ld_x32(ta, v);
+                tmem_ld_x32(ta, vv);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                  v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha_sh[32 * h2 + j]);
-                tmem_st_x32(ta, v);
+                  vv[j] = __float_as_uint(__uint_as_float(vv[j]) * alpha_sh[32 * h2 + j]);
+                tmem_st_x32(ta, vv);
               }
             }
             tmem_wait_st();
@@ -436,10 +454,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
         // ---------------- epilogue for this piece
         bool bad = !mbar_wait(smem_u32(&o_full), pc & 1, &abort_sh, P.status);
-        if (srow) {
-          const bool has = row_ok && l > 0.0f;
-          inv_l_sh[c] = has ? 1.0f / l : 0.0f;
-        }
+        l += __shfl_xor_sync(0xffffffffu, l, 2);  // even + odd halves of the row sum
+        if (owner) inv_l_sh[srow_c] = (row_ok && l > 0.0f) ? 1.0f / l : 0.0f;
         if (bar_any(1, 128, bad)) { fail = true; break; }
         tc_fence_after();
         const int nsplit = P.seq_nsplit[b];
@@ -501,13 +517,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&o_free));
         named_bar_sync(1, 128);
-        if (row_ok) {
+        if (owner && row_ok) {
           const float lse2 = (l > 0.0f) ? m_used + __log2f(l) : -INFINITY;
           if (nsplit > 1) {
-            P.lpart[part_base + c] = lse2 * kLn2;
+            P.lpart[part_base + srow_c] = lse2 * kLn2;
           } else {
-            const float corr_tot = corr_sh[0][c] + corr_sh[1][c] + corr_sh[2][c] + corr_sh[3][c];
-            P.lse[row_base + c] = lse2 * kLn2 + P.scale * corr_tot;
+            const float corr_tot = corr_sh[0][srow_c] + corr_sh[1][srow_c] + corr_sh[2][srow_c] +
+                                   corr_sh[3][srow_c];
+            P.lse[row_base + srow_c] = lse2 * kLn2 + P.scale * corr_tot;
           }
         }
         named_bar_sync(1, 128);
