@@ -125,9 +125,14 @@ int mla_decode_run(const mla_decode_dims* dims, const void* q, const void* kv_ca
 /* The four steps of mla_decode_run as separate calls, in this order, on one
  * workspace after mla_decode_plan (for profiling one step at a time).
  *   absorb:     q, w_uk            -> q_lat (bf16 hi and lo parts, workspace)
- *   attend:     q_lat, cache, ...  -> o_lat + lse for unsplit sequences,
- *                                     fp32 partials for split ones
- *   combine:    partials           -> o_lat + lse for split sequences
+ *   attend:     q_lat, cache, ...  -> o_lat + lse (from the bf16 part of q_lat)
+ *                                     for unsplit sequences, fp32 partials for
+ *                                     split ones
+ *   combine:    partials           -> o_lat + lse for split sequences; then
+ *                                     every row's lse += scale * (q_lo . o_lat),
+ *                                     the first-order correction for the bf16
+ *                                     rounding of q_lat (lse is final only
+ *                                     after this step)
  *   up_project: o_lat, w_uv        -> out                                   */
 int mla_decode_absorb(const mla_decode_dims* dims, const void* q, const void* w_uk,
                       void* workspace, size_t workspace_bytes, void* stream);

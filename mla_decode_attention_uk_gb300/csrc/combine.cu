@@ -6,10 +6,15 @@
 //   lse = ln sum_s exp(lse_s),   o = sum_s exp(lse_s - lse) o_s,
 // the split-KV decomposition of the FlashAttention family that FlashMLA
 // credits ("DeepSeek publica FlashMLA como codigo abierto").  The merged o is
-// stored as bf16 o_lat for the W_UV bmm; lse gets the first-order correction
-// scale * (q_lo . o) for the bf16 rounding of the absorbed query.
+// stored as bf16 o_lat for the W_UV bmm.
+//
+// Every row's lse (split or not) then gets the first-order correction
+// scale * (q_lo . o): the attention step scored keys with the bf16 part of the
+// absorbed query, q_lat = hi + q_lo, and d lse / d q_lat = scale * o, so adding
+// scale * (q_lo . o) restores the scores of the full-precision query up to
+// second order in q_lo (|q_lo| <= 2^-9 |q_lat|).
 // One warp per query row; each lane owns 16 of the 512 latent columns and
-// moves them with 16-byte vector loads and 8-byte vector stores.
+// moves them with 16-byte vector loads.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,8 +36,31 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
   const int b = blockIdx.y;
   const int r = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  if (r >= TH) return;
   const int ns = seq_nsplit[b];
-  if (ns <= 1 || r >= TH) return;
+  const size_t row = static_cast<size_t>(b) * TH + r;
+  if (ns <= 1) {
+    // Unsplit: o_lat and lse were written by the attention step.
+    const uint4* o4 = reinterpret_cast<const uint4*>(olat + row * kLora) + lane * 2;
+    const uint4* l4 = reinterpret_cast<const uint4*>(qlo + row * kLora) + lane * 2;
+    float corr = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint4 ov = o4[q], lv = l4[q];
+      const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+      const uint32_t lw[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(&ow[e]);
+        const __nv_bfloat162 l2 = *reinterpret_cast<const __nv_bfloat162*>(&lw[e]);
+        corr += __low2float(l2) * __low2float(o2) + __high2float(l2) * __high2float(o2);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) corr += __shfl_xor_sync(0xffffffffu, corr, o);
+    if (lane == 0) lse_out[row] += scale * corr;
+    return;
+  }
   const int slot0 = seq_slot[b];
   const WsLayout L = make_layout(B, T, H, header->num_ranges);
   const float* __restrict__ opart = reinterpret_cast<const float*>(ws + L.opart);
@@ -65,7 +93,6 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
     }
   }
 
-  const size_t row = static_cast<size_t>(b) * TH + r;
   float corr = 0.0f;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {

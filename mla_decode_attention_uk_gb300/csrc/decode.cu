@@ -25,12 +25,11 @@
 //   * PV on tcgen05, transposed: O^T[latent, row] += C^T[latent, key] P^T[key, row]
 //     with the chunk slot read MN-major as the A operand (M = 128 latent, four
 //     MMAs for 512) and N = 64 rows; O^T lives in 256 TMEM columns.
-//   * Epilogue (warps 4-7): O / l to bf16 o_lat plus lse for unsplit sequences
-//     (with the first-order correction lse += scale * (q_lo . o) for the bf16
-//     rounding of the absorbed query), or fp32 partials for split ones.
-// Warp roles: 0 TMA producer, 1 MMA issuer, 2 TMEM owner, 3 idle, 4-7 softmax
-// and epilogue.  The MMA issuer works from precomputed descriptors so one
-// instruction costs an add and the issue itself.
+//   * Epilogue (warps 4-7): O / l to bf16 o_lat plus lse for unsplit sequences,
+//     or fp32 partials for split ones.
+// Warp roles: 0 TMA producer, 1 QK^T issuer, 2 TMEM owner, 3 PV issuer, 4-7
+// softmax and epilogue.  The issuers work from precomputed descriptors so one
+// MMA costs an add and the issue itself.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -47,6 +46,7 @@ constexpr int kChunk = 32;                         // keys per streamed chunk
 constexpr int kChunkBox = kChunk * 128;            // one 32 x 64 bf16 box: 4 KB
 constexpr int kSlotBytes = kBoxes * kChunkBox;     // 36 KB
 constexpr int kMaxSlots = 6;
+constexpr int kSBufs = 4;                          // S accumulators (32 TMEM columns each)
 constexpr int kPTBytes = 64 * 128;                 // P^T: 64 rows x (up to 64 keys) bf16
 constexpr int kDynSmemMax = 232448 - 2048;         // opt-in limit minus static smem budget
 constexpr uint32_t kTmemCols = 512;
@@ -129,12 +129,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, q_free, slot_full[kMaxSlots], slot_empty[kMaxSlots],
-      s_full[2], s_free[2], p_full[2], p_free[2], o_full, o_free, drain_bar;
+      s_full[4], s_free[4], p_full[2], p_free[2], o_full, o_free, drain_bar[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ float alpha_sh[64];
   __shared__ float inv_l_sh[64];
-  __shared__ float corr_sh[4][64];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x % P.tiles;
@@ -166,7 +165,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(smem_u32(&slot_full[i]), 1);
       mbar_init(smem_u32(&slot_empty[i]), CS);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
       mbar_init(smem_u32(&s_free[i]), 4);
     }
@@ -176,7 +175,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
     mbar_init(smem_u32(&o_full), 1);
     mbar_init(smem_u32(&o_free), 4);
-    mbar_init(smem_u32(&drain_bar), 1);
+    mbar_init(smem_u32(&drain_bar[0]), 1);
+    mbar_init(smem_u32(&drain_bar[1]), 1);
     abort_sh = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -243,8 +243,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues QK^T and runs ahead over the S buffers; warp 3 issues PV
+    // as soon as the softmax has written P.  Each commits its own MMAs.
     if (elect_one()) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(64, kChunk, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 64, true, false);
@@ -255,79 +257,77 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const uint64_t dpv0 = sdesc_sw128(sSlot0, kChunkBox, 1024);
       const uint64_t dpt0 = sdesc_sw128(sPT, 16, 1024);
       const uint32_t qbox16 = q_box_bytes >> 4;
+      const bool is_qk = warp == 1;
       int g = 0, pc = 0;
       bool ok = true;
-      auto issue_pv = [&](int gg, bool first) -> bool {
-        const int pb2 = gg & 1;  // P^T half used by this chunk
-        if (!mbar_wait(smem_u32(&p_full[pb2]), (gg >> 1) & 1, &abort_sh, P.status)) return false;
-        if (first && pc > 0 && !mbar_wait(smem_u32(&o_free), (pc - 1) & 1, &abort_sh, P.status))
-          return false;
-        tc_fence_after();
-        const int s = gg % NS;
-        const uint64_t ad0 = dpv0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
-        const uint64_t bd0 = dpt0 + static_cast<uint64_t>(pb2 * 4);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-#pragma unroll
-          for (int kk = 0; kk < kChunk / 16; ++kk) {
-            umma_bf16(tmem + kTmemO + 64 * m, ad0 + ((2 * m * kChunkBox + kk * 2048) >> 4),
-                      bd0 + kk * 2, idesc_pv, !(first && kk == 0));
-          }
-        }
-        umma_commit(smem_u32(&p_free[pb2]));
-        if (CS == 1)
-          umma_commit(smem_u32(&slot_empty[s]));
-        else
-          umma_commit_mc(smem_u32(&slot_empty[s]), cmask);
-        return true;
-      };
       for (int k = k0; k < R && ok; k += G) {
         PieceWalker w(P, k);
         int b, pb, pe;
         while (ok && w.next(P, b, pb, pe)) {
-          if (!mbar_wait(smem_u32(&q_full), pc & 1, &abort_sh, P.status)) {
-            ok = false;
-            break;
-          }
           const ChunkRange cr(P.seq_len_eff[b], pb, pe);
           const int nc = cr.nchunks;
-          for (int i = 0; i < nc; ++i, ++g) {
-            const int s = g % NS, sb = g & 1;
-            if (!mbar_wait(smem_u32(&slot_full[s]), (g / NS) & 1, &abort_sh, P.status) ||
-                (g >= 2 &&
-                 !mbar_wait(smem_u32(&s_free[sb]), ((g >> 1) - 1) & 1, &abort_sh, P.status))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t bd0 = dslot0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
-#pragma unroll
-            for (int j = 0; j < kBoxes; ++j) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                umma_bf16(tmem + kChunk * sb, dq0 + (j * qbox16 + kk * 2),
-                          bd0 + ((j * kChunkBox) >> 4) + kk * 2, idesc_qk, (j | kk) != 0);
+          if (is_qk) {
+            if (!mbar_wait(smem_u32(&q_full), pc & 1, &abort_sh, P.status)) { ok = false; break; }
+            for (int i = 0; i < nc; ++i, ++g) {
+              const int s = g % NS, sb = g % kSBufs;
+              if (!mbar_wait(smem_u32(&slot_full[s]), (g / NS) & 1, &abort_sh, P.status) ||
+                  (g >= kSBufs && !mbar_wait(smem_u32(&s_free[sb]), ((g / kSBufs) - 1) & 1,
+                                             &abort_sh, P.status))) {
+                ok = false;
+                break;
               }
+              tc_fence_after();
+              const uint64_t bd0 = dslot0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
+#pragma unroll
+              for (int j = 0; j < kBoxes; ++j) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  umma_bf16(tmem + kChunk * sb, dq0 + (j * qbox16 + kk * 2),
+                            bd0 + ((j * kChunkBox) >> 4) + kk * 2, idesc_qk, (j | kk) != 0);
+                }
+              }
+              umma_commit(smem_u32(&s_full[sb]));
+              if (i == nc - 1) umma_commit(smem_u32(&q_free));
             }
-            umma_commit(smem_u32(&s_full[sb]));
-            if (i == nc - 1) umma_commit(smem_u32(&q_free));
-            if (i > 0 && !issue_pv(g - 1, i - 1 == 0)) {
-              ok = false;
-              break;
+          } else {
+            for (int i = 0; i < nc; ++i, ++g) {
+              const int pb2 = g & 1;  // P^T half used by this chunk
+              const bool first = i == 0;
+              if (!mbar_wait(smem_u32(&p_full[pb2]), (g >> 1) & 1, &abort_sh, P.status) ||
+                  (first && pc > 0 &&
+                   !mbar_wait(smem_u32(&o_free), (pc - 1) & 1, &abort_sh, P.status))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const int s = g % NS;
+              const uint64_t ad0 = dpv0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
+              const uint64_t bd0 = dpt0 + static_cast<uint64_t>(pb2 * 4);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                for (int kk = 0; kk < kChunk / 16; ++kk) {
+                  umma_bf16(tmem + kTmemO + 64 * m, ad0 + ((2 * m * kChunkBox + kk * 2048) >> 4),
+                            bd0 + kk * 2, idesc_pv, !(first && kk == 0));
+                }
+              }
+              umma_commit(smem_u32(&p_free[pb2]));
+              if (CS == 1)
+                umma_commit(smem_u32(&slot_empty[s]));
+              else
+                umma_commit_mc(smem_u32(&slot_empty[s]), cmask);
             }
+            if (!ok) break;
+            umma_commit(smem_u32(&o_full));
           }
           if (!ok) break;
-          if (!issue_pv(g - 1, nc == 1)) {
-            ok = false;
-            break;
-          }
-          umma_commit(smem_u32(&o_full));
           ++pc;
         }
       }
-      // Drain the tensor pipe before TMEM is released.
-      umma_commit(smem_u32(&drain_bar));
-      mbar_wait_drain(smem_u32(&drain_bar), 0, P.status);
+      // Drain this issuer's MMAs before TMEM is released.
+      const uint32_t db = smem_u32(is_qk ? &drain_bar[0] : &drain_bar[1]);
+      umma_commit(db);
+      mbar_wait_drain(db, 0, P.status);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
@@ -353,9 +353,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const ChunkRange cr(L, pb, pe);
         const int nc = cr.nchunks;
         for (int i = 0; i < nc; ++i, ++g) {
-          const int sb = g & 1;
+          const int sb = g % kSBufs;
           bool need = false;
-          bool bad = !mbar_wait(smem_u32(&s_full[sb]), (g >> 1) & 1, &abort_sh, P.status);
+          bool bad = !mbar_wait(smem_u32(&s_full[sb]), (g / kSBufs) & 1, &abort_sh, P.status);
           bad = __any_sync(0xffffffffu, bad);  // tcgen05.ld below is warp-collective
           uint32_t v[kChunk / 2];
           if (!bad) {
@@ -464,28 +464,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const size_t part_base =
             nsplit > 1 ? (static_cast<size_t>(P.seq_slot[b] + split) * TH + tile * kTileRows) : 0;
         const int rows_here = min(kTileRows, TH - tile * kTileRows);
-        const __nv_bfloat16* __restrict__ qlo = P.qlo;
         __nv_bfloat16* __restrict__ olat = P.olat;
         float* __restrict__ opart = P.opart;
 #pragma unroll 1
-        for (int h2 = 0; h2 < 2; ++h2) {
-          float corr[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) corr[j] = 0.0f;
+        for (int m = 0; m < 4; ++m) {
+          const int lat = 128 * m + 32 * wq + lane;
 #pragma unroll 1
-          for (int m = 0; m < 4; ++m) {
-            const int lat = 128 * m + 32 * wq + lane;
-            // Issue this block's q_lo loads before any store so they overlap.
-            float lo[32];
-            if (nsplit <= 1) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int cc = 32 * h2 + j;
-                lo[j] = cc < rows_here
-                            ? __bfloat162float(qlo[(row_base + cc) * kLora + lat])
-                            : 0.0f;
-              }
-            }
+          for (int h2 = 0; h2 < 2; ++h2) {
             uint32_t v[32];
             tmem_ld_x32(tmem + lane_off + kTmemO + 64 * m + 32 * h2, v);
             tmem_wait_ld();
@@ -494,22 +479,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               const int cc = 32 * h2 + j;
               if (cc < rows_here) {
                 const float val = __uint_as_float(v[j]) * inv_l_sh[cc];
-                if (nsplit > 1) {
+                if (nsplit > 1)
                   opart[(part_base + cc) * kLora + lat] = val;
-                } else {
+                else
                   olat[(row_base + cc) * kLora + lat] = __float2bfloat16_rn(val);
-                  corr[j] += lo[j] * val;
-                }
               }
-            }
-          }
-          if (nsplit <= 1) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              float t = corr[j];
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-              if (lane == j) corr_sh[wq][32 * h2 + j] = t;
             }
           }
         }
@@ -518,14 +492,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (lane == 0) mbar_arrive(smem_u32(&o_free));
         named_bar_sync(1, 128);
         if (owner && row_ok) {
+          // Natural-log LSE of this key range; the combine step adds the
+          // first-order correction for the bf16 rounding of the query.
           const float lse2 = (l > 0.0f) ? m_used + __log2f(l) : -INFINITY;
-          if (nsplit > 1) {
+          if (nsplit > 1)
             P.lpart[part_base + srow_c] = lse2 * kLn2;
-          } else {
-            const float corr_tot = corr_sh[0][srow_c] + corr_sh[1][srow_c] + corr_sh[2][srow_c] +
-                                   corr_sh[3][srow_c];
-            P.lse[row_base + srow_c] = lse2 * kLn2 + P.scale * corr_tot;
-          }
+          else
+            P.lse[row_base + srow_c] = lse2 * kLn2;
         }
         named_bar_sync(1, 128);
         ++pc;
