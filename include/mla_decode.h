@@ -163,6 +163,33 @@ const char* mla_decode_status_string(int status);
 int mla_decode_workspace_offsets(const mla_decode_dims* dims, int32_t num_ranges,
                                  int64_t* offsets, int32_t n);
 
+/* Plan + run without a caller-provided workspace, for callers that cannot
+ * allocate device memory: for example a custom operator inside a serving
+ * engine whose memory pool owns the device and passes an operator only its
+ * inputs and outputs, or code running under a stream capture whose mode
+ * forbids new allocations.  The pages describing the method have no
+ * counterpart to this call; it is a packaging choice of this library.
+ *
+ * Arguments are those of mla_decode_run minus the workspace.  Scratch comes
+ * from a fixed 32 MiB array in statically allocated device memory, which every
+ * GPU that loads the library holds until the process exits; the call makes no
+ * allocation of any kind.  If mla_decode_workspace_size(dims) exceeds 32 MiB
+ * it returns MLA_DECODE_WORKSPACE_TOO_SMALL and enqueues nothing.  On a
+ * 152-SM GB300 that admits up to 32 query rows per sequence (T * H <= 32, e.g.
+ * 16 heads with one or two query tokens), up to roughly 130-460 sequences.  The first call on each device looks up that device's copy of the
+ * array (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  All calls on a device share the one array, which keeps the last
+ * call's contents: calls whose work overlaps on the GPU (other streams, other
+ * host threads) race and must be serialised by the caller.  Device-side
+ * bounds errors are recorded in the shared array but cannot be queried
+ * through this entry point; use mla_decode_run with a workspace and
+ * mla_decode_check when that matters. */
+int mla_decode_run_static_scratch(const mla_decode_dims* dims, const void* q,
+                                  const void* kv_cache, const int32_t* block_table,
+                                  const int32_t* seq_lens, const void* w_uk,
+                                  const void* w_uv, float softmax_scale, void* out,
+                                  float* lse, void* stream);
+
 /* Number of kernels one mla_decode_run enqueues (for launch accounting). */
 int mla_decode_kernels_per_run(void);
 

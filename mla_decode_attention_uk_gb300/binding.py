@@ -22,7 +22,8 @@ ENTRY_POINTS = (
     "mla_decode_workspace_size", "mla_decode_workspace_size_ex", "mla_decode_plan",
     "mla_decode_plan_ex", "mla_decode_run", "mla_decode_absorb", "mla_decode_attend",
     "mla_decode_combine", "mla_decode_up_project", "mla_decode_check", "mla_decode_status_string",
-    "mla_decode_workspace_offsets", "mla_decode_kernels_per_run")
+    "mla_decode_workspace_offsets", "mla_decode_kernels_per_run",
+    "mla_decode_run_static_scratch")
 
 
 class Dims(ctypes.Structure):
@@ -64,6 +65,7 @@ def lib():
         L.mla_decode_status_string.argtypes = [ctypes.c_int]
         L.mla_decode_status_string.restype = ctypes.c_char_p
         L.mla_decode_workspace_offsets.argtypes = [D, i32, ctypes.POINTER(ctypes.c_int64), i32]
+        L.mla_decode_run_static_scratch.argtypes = [D, P, P, P, P, P, P, ctypes.c_float, P, P, P]
         for n in ENTRY_POINTS:
             if n != "mla_decode_status_string":
                 getattr(L, n).restype = ctypes.c_int
