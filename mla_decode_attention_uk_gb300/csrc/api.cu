@@ -278,7 +278,7 @@ int mla_decode_attend(const mla_decode_dims* d, const void* kv_cache, const int3
   if (!make_map(&tm_q, at<void>(ws, L.qlat), rows, kDqk, kDqk, kBoxCols,
                 decode_q_box_rows(d->q_len, d->num_heads), false) ||
       !make_map(&tm_c, kv_cache, static_cast<uint64_t>(d->num_pages) * kPage, kDqk, kDqk,
-                kBoxCols, 32, true))
+                kBoxCols, kPage, true))
     return MLA_DECODE_CUDA_ERROR;
   int groups = 0;
   rc = default_ranges(d, &groups);

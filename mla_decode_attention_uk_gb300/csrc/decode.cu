@@ -10,21 +10,23 @@
 // ranges cut by the planner are merged later by their log-sum-exp.
 //
 // GB300 mapping (one CTA = 64 query rows of one sequence, one work range):
-//   * Keys stream in 32-token chunks (half a page): the TMA producer gathers a
-//     chunk as 9 boxes of 32 x 64 bf16 (128B swizzle) into a ring of 4-5 slots
-//     of 36 KB, looking the physical page up in the block table.  When the
+//   * Keys stream page by page: the TMA producer gathers a 64-token page as 9
+//     boxes of 64 x 64 bf16 (128B swizzle) into a ring of 72 KB slots, looking
+//     the physical page up in the block table.  When the
 //     query rows of a sequence span 2 or 4 CTAs, those CTAs form a cluster and
 //     each loads a share of every chunk with TMA multicast, so a chunk leaves
 //     L2 once per cluster.
-//   * QK^T on tcgen05: S[row, key] = sum_576 Q[row] C[key]; M = 64 rows, N = 32
+//   * QK^T on tcgen05: S[row, key] = sum_576 Q[row] C[key]; M = 64 rows, N = 64
 //     keys, fp32 in TMEM (an M = 64 accumulator puts 16 rows in each 32-lane
-//     quarter), two S buffers.
+//     quarter), two S buffers.  A whole page per MMA keeps the shared-memory
+//     reads of the query tile at one pass per 64 keys.
 //   * Softmax (warps 4-7, 16 rows each, two threads per row holding the even
 //     and odd keys): exp2 with a lazily updated running max (rescale only
 //     when the max grows by more than 2^8), P written to shared memory as bf16.
 //   * PV on tcgen05, transposed: O^T[latent, row] += C^T[latent, key] P^T[key, row]
-//     with the chunk slot read MN-major as the A operand (M = 128 latent, four
-//     MMAs for 512) and N = 64 rows; O^T lives in 256 TMEM columns.
+//     with the page slot read MN-major as the A operand (M = 128 latent, four
+//     MMAs for 512) and N = 64 rows; O^T lives in 256 TMEM columns.  P^T is
+//     double-buffered when the query tile is small enough to leave room.
 //   * Epilogue (warps 4-7): O / l to bf16 o_lat plus lse for unsplit sequences,
 //     or fp32 partials for split ones.
 // Warp roles: 0 TMA producer, 1 QK^T issuer, 2 TMEM owner, 3 PV issuer, 4-7
@@ -42,12 +44,13 @@ namespace mla {
 namespace {
 
 constexpr int kDecThreads = 256;
-constexpr int kChunk = 32;                         // keys per streamed chunk
-constexpr int kChunkBox = kChunk * 128;            // one 32 x 64 bf16 box: 4 KB
-constexpr int kSlotBytes = kBoxes * kChunkBox;     // 36 KB
-constexpr int kMaxSlots = 6;
-constexpr int kSBufs = 4;                          // S accumulators (32 TMEM columns each)
-constexpr int kPTBytes = 64 * 128;                 // P^T: 64 rows x (up to 64 keys) bf16
+constexpr int kChunk = 64;                         // keys per streamed chunk (one page)
+constexpr int kChunkBox = kChunk * 128;            // one 64 x 64 bf16 box: 8 KB
+constexpr int kSlotBytes = kBoxes * kChunkBox;     // 72 KB
+constexpr int kMaxSlots = 4;
+constexpr int kSBufs = 2;                          // S accumulators (64 TMEM columns each)
+constexpr int kPTBytes = 64 * 128;                 // one P^T buffer: 64 rows x 64 keys bf16
+constexpr int kMaxPT = 2;
 constexpr int kDynSmemMax = 232448 - 2048;         // opt-in limit minus static smem budget
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 128;                   // O^T blocks at 128 + 64 m
@@ -70,7 +73,7 @@ struct DecodeParams {
   float* opart;              // [slots, T*H, 512]
   float* lpart;              // [slots, T*H]
   int32_t* status;
-  int B, T, H, max_pages, num_pages, tiles, q_box_rows, num_slots, cluster;
+  int B, T, H, max_pages, num_pages, tiles, q_box_rows, num_slots, num_pt, cluster;
   float scale, scale_log2;
 };
 
@@ -110,18 +113,12 @@ struct PieceWalker {
   }
 };
 
-// Chunks of a piece: two per page, except a last page whose keys all fall in
-// its first half.  Chunk i of the piece covers keys key0(i) .. key0(i) + 31.
+// Chunks of a piece: one per page; chunk i covers keys key0(i) .. key0(i) + 63.
 struct ChunkRange {
   int pbeg, nchunks;
-  __device__ ChunkRange(int L, int pb, int pe) : pbeg(pb) {
-    nchunks = 2 * (pe - pb);
-    const int last_page = (L - 1) / kPage;
-    if (pe - 1 == last_page && L - last_page * kPage <= kChunk) nchunks -= 1;
-  }
-  __device__ int page(int i) const { return pbeg + (i >> 1); }
-  __device__ int half(int i) const { return i & 1; }
-  __device__ int key0(int i) const { return pbeg * kPage + i * kChunk; }
+  __device__ ChunkRange(int /*L*/, int pb, int pe) : pbeg(pb), nchunks(pe - pb) {}
+  __device__ int page(int i) const { return pbeg + i; }
+  __device__ int key0(int i) const { return (pbeg + i) * kPage; }
 };
 
 __global__ void __launch_bounds__(kDecThreads, 1)
@@ -129,7 +126,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, q_free, slot_full[kMaxSlots], slot_empty[kMaxSlots],
-      s_full[4], s_free[4], p_full[2], p_free[2], o_full, o_free, drain_bar[2];
+      s_full[kSBufs], s_free[kSBufs], p_full[kMaxPT], p_free[kMaxPT], o_full, o_free,
+      drain_bar[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ float alpha_sh[64];
@@ -142,6 +140,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int R = P.header->num_ranges;
   const int TH = P.T * P.H;
   const int NS = P.num_slots;
+  const int NPT = P.num_pt;                       // P^T buffers (1 or 2)
   const int CS = P.cluster;                       // CTAs sharing each chunk (1, 2 or 4)
   const int crank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const uint16_t cmask = static_cast<uint16_t>((1u << CS) - 1u);
@@ -169,7 +168,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(smem_u32(&s_full[i]), 1);
       mbar_init(smem_u32(&s_free[i]), 4);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NPT; ++i) {
       mbar_init(smem_u32(&p_full[i]), 4);
       mbar_init(smem_u32(&p_free[i]), 1);
     }
@@ -220,16 +219,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               ok = false;
               break;
             }
-            if (cr.half(i) == 0 || i == 0) {
-              pg = __ldg(P.block_table + static_cast<size_t>(b) * P.max_pages + cr.page(i));
-              if (pg < 0 || pg >= P.num_pages) {
-                atomicCAS(P.status, 0, MLA_STATUS_BOUNDS);
-                pg = 0;
-              }
+            pg = __ldg(P.block_table + static_cast<size_t>(b) * P.max_pages + cr.page(i));
+            if (pg < 0 || pg >= P.num_pages) {
+              atomicCAS(P.status, 0, MLA_STATUS_BOUNDS);
+              pg = 0;
             }
             const uint32_t dst = sSlot0 + s * kSlotBytes;
             const uint32_t fb = smem_u32(&slot_full[s]);
-            const int row = pg * kPage + cr.half(i) * kChunk;
+            const int row = pg * kPage;
             mbar_expect_tx(fb, kSlotBytes);
             if (CS == 1) {
               for (int j = 0; j < kBoxes; ++j)
@@ -291,9 +288,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
           } else {
             for (int i = 0; i < nc; ++i, ++g) {
-              const int pb2 = g & 1;  // P^T half used by this chunk
+              const int pb2 = g % NPT;  // P^T buffer used by this chunk
               const bool first = i == 0;
-              if (!mbar_wait(smem_u32(&p_full[pb2]), (g >> 1) & 1, &abort_sh, P.status) ||
+              if (!mbar_wait(smem_u32(&p_full[pb2]), (g / NPT) & 1, &abort_sh, P.status) ||
                   (first && pc > 0 &&
                    !mbar_wait(smem_u32(&o_free), (pc - 1) & 1, &abort_sh, P.status))) {
                 ok = false;
@@ -302,7 +299,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               tc_fence_after();
               const int s = g % NS;
               const uint64_t ad0 = dpv0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
-              const uint64_t bd0 = dpt0 + static_cast<uint64_t>(pb2 * 4);
+              const uint64_t bd0 = dpt0 + static_cast<uint64_t>((pb2 * kPTBytes) >> 4);
 #pragma unroll
               for (int m = 0; m < 4; ++m) {
 #pragma unroll
@@ -360,7 +357,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           uint32_t v[kChunk / 2];
           if (!bad) {
             tc_fence_after();
-            tmem_ld_16x64b_x16(tmem + lane_off + kChunk * sb, v);
+            tmem_ld_16x64b_x32(tmem + lane_off + kChunk * sb, v);
             tmem_wait_ld();
           }
           tc_fence_before();
@@ -391,27 +388,25 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             l = l * alpha + sum;
             if (owner) alpha_sh[srow_c] = alpha;
-            // Pair up neighbouring keys: the even-key thread writes keys 0..15
-            // of the chunk, the odd-key thread keys 16..31.
-            uint32_t packed[8];
+            // Pair up neighbouring keys: the even-key thread writes keys 0..31
+            // of the chunk, the odd-key thread keys 32..63.
+            uint32_t packed[16];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float send = par ? p[q] : p[8 + q];
+            for (int q = 0; q < 16; ++q) {
+              const float send = par ? p[q] : p[16 + q];
               const float recv = __shfl_xor_sync(0xffffffffu, send, 2);
-              packed[q] = par ? pack_bf16x2(recv, p[8 + q]) : pack_bf16x2(p[q], recv);
+              packed[q] = par ? pack_bf16x2(recv, p[16 + q]) : pack_bf16x2(p[q], recv);
             }
-            // P^T is double-buffered in the two 64-byte halves of each
-            // 128-byte swizzled row; this half is free once the PV of the
-            // chunk before last has finished.
-            const int pb2 = g & 1;
-            if (g >= 2 && !mbar_wait(smem_u32(&p_free[pb2]), ((g >> 1) - 1) & 1, &abort_sh,
-                                     P.status))
+            // P^T buffer pb2 is free once the PV that last read it has finished.
+            const int pb2 = g % NPT;
+            if (g >= NPT && !mbar_wait(smem_u32(&p_free[pb2]), ((g / NPT) - 1) & 1, &abort_sh,
+                                       P.status))
               bad = true;
             if (!bad) {
-              const uint32_t rowaddr = sPT + srow_c * 128;
+              const uint32_t rowaddr = sPT + pb2 * kPTBytes + srow_c * 128;
 #pragma unroll
-              for (int q = 0; q < 2; ++q) {
-                const int lchunk = 4 * pb2 + 2 * par + q;
+              for (int q = 0; q < 4; ++q) {
+                const int lchunk = 4 * par + q;
                 st_shared_v4(rowaddr + ((lchunk ^ (srow_c & 7)) << 4), packed[4 * q],
                              packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
               }
@@ -424,7 +419,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // quarters) once the previous chunk's PV has landed.
             bool f = *static_cast<volatile int*>(&abort_sh) != 0;
             if (!f && g >= 1 &&
-                !mbar_wait(smem_u32(&p_free[(g - 1) & 1]), ((g - 1) >> 1) & 1, &abort_sh,
+                !mbar_wait(smem_u32(&p_free[(g - 1) % NPT]), ((g - 1) / NPT) & 1, &abort_sh,
                            P.status))
               f = true;
             if (bar_any(1, 128, f)) { fail = true; break; }
@@ -448,7 +443,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             named_bar_sync(1, 128);  // alpha_sh is rewritten by the next chunk
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&p_full[g & 1]));
+          if (lane == 0) mbar_arrive(smem_u32(&p_full[g % NPT]));
         }
         if (fail) break;
 
@@ -523,14 +518,20 @@ int decode_q_box_rows(int T, int H) {
   const int r = T * H;
   return r >= kTileRows ? kTileRows : ((r + 7) / 8) * 8;
 }
+// Page slots and P^T buffers that fit next to the query tile: two P^T
+// buffers when two page slots still fit, else one.
+int decode_num_pt(int T, int H) {
+  const int q_bytes = kBoxes * decode_q_box_rows(T, H) * 128;
+  return (kDynSmemMax - 1024 - q_bytes - 2 * kPTBytes) / kSlotBytes >= 2 ? 2 : 1;
+}
 int decode_num_slots(int T, int H) {
   const int q_bytes = kBoxes * decode_q_box_rows(T, H) * 128;
-  int ns = (kDynSmemMax - 1024 - q_bytes - kPTBytes) / kSlotBytes;
+  int ns = (kDynSmemMax - 1024 - q_bytes - decode_num_pt(T, H) * kPTBytes) / kSlotBytes;
   return ns > kMaxSlots ? kMaxSlots : ns;
 }
 int decode_smem_bytes(int T, int H) {
   return 1024 + kBoxes * decode_q_box_rows(T, H) * 128 + decode_num_slots(T, H) * kSlotBytes +
-         kPTBytes;
+         decode_num_pt(T, H) * kPTBytes;
 }
 // CTAs that share each key chunk through TMA multicast (a cluster).
 int decode_cluster_size(int T, int H) {
@@ -603,6 +604,7 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
   P.tiles = decode_tiles(T, H);
   P.q_box_rows = decode_q_box_rows(T, H);
   P.num_slots = decode_num_slots(T, H);
+  P.num_pt = decode_num_pt(T, H);
   P.cluster = decode_cluster_size(T, H);
   P.scale = scale;
   P.scale_log2 = scale * 1.4426950408889634f;
