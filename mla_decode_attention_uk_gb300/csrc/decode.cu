@@ -29,8 +29,8 @@
 //     double-buffered when the query tile is small enough to leave room.
 //   * Epilogue (warps 4-7): O / l to bf16 o_lat plus lse for unsplit sequences,
 //     or fp32 partials for split ones.
-// Warp roles: 0 TMA producer, 1 QK^T issuer, 2 TMEM owner, 3 PV issuer, 4-7
-// softmax and epilogue.  The issuers work from precomputed descriptors so one
+// Warp roles: 0 TMA producer, 1-2 QK^T issuers (even / odd pages; warp 2 also
+// owns TMEM), 3 PV issuer, 4-7 softmax and epilogue.  The issuers work from precomputed descriptors so one
 // MMA costs an add and the issue itself.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -127,7 +127,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, q_free, slot_full[kMaxSlots], slot_empty[kMaxSlots],
       s_full[kSBufs], s_free[kSBufs], p_full[kMaxPT], p_free[kMaxPT], o_full, o_free,
-      drain_bar[2];
+      drain_bar[3];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ float alpha_sh[64];
@@ -159,7 +159,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&q_full), 1);
-    mbar_init(smem_u32(&q_free), 1);
+    mbar_init(smem_u32(&q_free), 2);
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&slot_full[i]), 1);
       mbar_init(smem_u32(&slot_empty[i]), CS);
@@ -174,8 +174,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
     mbar_init(smem_u32(&o_full), 1);
     mbar_init(smem_u32(&o_free), 4);
-    mbar_init(smem_u32(&drain_bar[0]), 1);
-    mbar_init(smem_u32(&drain_bar[1]), 1);
+    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&drain_bar[i]), 1);
     abort_sh = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -240,10 +239,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
       }
     }
-  } else if (warp == 1 || warp == 3) {
+  }
+  if (warp >= 1 && warp <= 3) {
     // ------------------------------------------------------------ MMA issuers
-    // Warp 1 issues QK^T and runs ahead over the S buffers; warp 3 issues PV
-    // as soon as the softmax has written P.  Each commits its own MMAs.
+    // Warps 1 and 2 issue QK^T for even and odd pages (a single issuing
+    // thread cannot keep the tensor pipe busy with M = 64 MMAs; two overlap),
+    // warp 3 issues PV as soon as the softmax has written P.  Each issuer
+    // commits its own MMAs.
     if (elect_one()) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(64, kChunk, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 64, true, false);
@@ -254,7 +256,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const uint64_t dpv0 = sdesc_sw128(sSlot0, kChunkBox, 1024);
       const uint64_t dpt0 = sdesc_sw128(sPT, 16, 1024);
       const uint32_t qbox16 = q_box_bytes >> 4;
-      const bool is_qk = warp == 1;
+      const bool is_qk = warp != 3;
+      const int qk_par = warp - 1;  // page parity handled by this QK issuer
       int g = 0, pc = 0;
       bool ok = true;
       for (int k = k0; k < R && ok; k += G) {
@@ -266,6 +269,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           if (is_qk) {
             if (!mbar_wait(smem_u32(&q_full), pc & 1, &abort_sh, P.status)) { ok = false; break; }
             for (int i = 0; i < nc; ++i, ++g) {
+              if ((g & 1) != qk_par) continue;
               const int s = g % NS, sb = g % kSBufs;
               if (!mbar_wait(smem_u32(&slot_full[s]), (g / NS) & 1, &abort_sh, P.status) ||
                   (g >= kSBufs && !mbar_wait(smem_u32(&s_free[sb]), ((g / kSBufs) - 1) & 1,
@@ -284,8 +288,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
               }
               umma_commit(smem_u32(&s_full[sb]));
-              if (i == nc - 1) umma_commit(smem_u32(&q_free));
             }
+            if (!ok) break;
+            // Both QK issuers release the query tile (count 2) once their
+            // MMAs of this piece have finished reading it.
+            umma_commit(smem_u32(&q_free));
           } else {
             for (int i = 0; i < nc; ++i, ++g) {
               const int pb2 = g % NPT;  // P^T buffer used by this chunk
@@ -322,7 +329,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
       }
       // Drain this issuer's MMAs before TMEM is released.
-      const uint32_t db = smem_u32(is_qk ? &drain_bar[0] : &drain_bar[1]);
+      const uint32_t db = smem_u32(&drain_bar[warp - 1]);
       umma_commit(db);
       mbar_wait_drain(db, 0, P.status);
     }
