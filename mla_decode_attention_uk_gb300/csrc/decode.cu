@@ -51,6 +51,7 @@ constexpr int kMaxSlots = 4;
 constexpr int kSBufs = 2;                          // S accumulators (64 TMEM columns each)
 constexpr int kPTBytes = 64 * 128;                 // one P^T buffer: 64 rows x 64 keys bf16
 constexpr int kMaxPT = 2;
+constexpr int kPrefetchPages = 4;                  // L2 prefetch distance, in pages
 constexpr int kDynSmemMax = 232448 - 2048;         // opt-in limit minus static smem budget
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 128;                   // O^T blocks at 128 + 64 m
@@ -211,21 +212,33 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           for (int j = 0; j < kBoxes; ++j)
             tma_load_2d(sQ + j * q_box_bytes, &tm_q, j * kBoxCols, qrow, smem_u32(&q_full));
           const ChunkRange cr(P.seq_len_eff[b], pb, pe);
-          int pg = 0;
+          const int32_t* bt_row = P.block_table + static_cast<size_t>(b) * P.max_pages;
+          // Pages are also prefetched into L2 kPrefetchPages ahead of their
+          // shared-memory load, so a slot refill mostly hits L2 instead of
+          // waiting a full HBM round trip.
+          auto page_of = [&](int i) {
+            int pg = __ldg(bt_row + cr.page(i));
+            if (pg < 0 || pg >= P.num_pages) {
+              atomicCAS(P.status, 0, MLA_STATUS_BOUNDS);
+              pg = 0;
+            }
+            return pg;
+          };
+          auto prefetch = [&](int i) {
+            const int row = page_of(i) * kPage;
+            for (int j = crank; j < kBoxes; j += CS) tma_prefetch_l2_2d(&tm_c, j * kBoxCols, row);
+          };
+          for (int i = 0; i < cr.nchunks && i < kPrefetchPages; ++i) prefetch(i);
           for (int i = 0; i < cr.nchunks; ++i, ++g) {
             const int s = g % NS, u = g / NS;
             if (u > 0 && !mbar_wait(smem_u32(&slot_empty[s]), (u - 1) & 1, &abort_sh, P.status)) {
               ok = false;
               break;
             }
-            pg = __ldg(P.block_table + static_cast<size_t>(b) * P.max_pages + cr.page(i));
-            if (pg < 0 || pg >= P.num_pages) {
-              atomicCAS(P.status, 0, MLA_STATUS_BOUNDS);
-              pg = 0;
-            }
+            if (i + kPrefetchPages < cr.nchunks) prefetch(i + kPrefetchPages);
+            const int row = page_of(i) * kPage;
             const uint32_t dst = sSlot0 + s * kSlotBytes;
             const uint32_t fb = smem_u32(&slot_full[s]);
-            const int row = pg * kPage;
             mbar_expect_tx(fb, kSlotBytes);
             if (CS == 1) {
               for (int j = 0; j < kBoxes; ++j)
@@ -372,14 +385,21 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           if (lane == 0) mbar_arrive(smem_u32(&s_free[sb]));
           if (!bad) {
             const int kb = cr.key0(i) + par;    // key of v[0]; v[j] is key kb + 2 j
-            float x[kChunk / 2];
-            float pmax = -INFINITY;
+            // Max over raw scores (scale > 0), masking only on a sequence's
+            // last page; then p = 2^(s * scale * log2 e - m) with one FFMA.
+            float vmax = -INFINITY;
+            if (kb + 2 * (kChunk / 2 - 1) < n_row) {
 #pragma unroll
-            for (int j = 0; j < kChunk / 2; ++j) {
-              x[j] = (kb + 2 * j < n_row) ? __uint_as_float(v[j]) * P.scale_log2 : -INFINITY;
-              pmax = fmaxf(pmax, x[j]);
+              for (int j = 0; j < kChunk / 2; ++j) vmax = fmaxf(vmax, __uint_as_float(v[j]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < kChunk / 2; ++j) {
+                if (kb + 2 * j >= n_row) v[j] = __float_as_uint(-INFINITY);
+                vmax = fmaxf(vmax, __uint_as_float(v[j]));
+              }
             }
-            pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, 2));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+            const float pmax = vmax * P.scale_log2;
             float alpha = 1.0f;
             if (pmax > m_used + kRescaleThreshold) {
               alpha = (m_used == -INFINITY) ? 0.0f : ex2_approx(m_used - pmax);
@@ -388,10 +408,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             float p[kChunk / 2];
             float sum = 0.0f;
+            if (m_used == -INFINITY) {
 #pragma unroll
-            for (int j = 0; j < kChunk / 2; ++j) {
-              p[j] = (x[j] == -INFINITY) ? 0.0f : ex2_approx(x[j] - m_used);
-              sum += p[j];
+              for (int j = 0; j < kChunk / 2; ++j) p[j] = 0.0f;
+            } else {
+              const float neg_m = -m_used;
+#pragma unroll
+              for (int j = 0; j < kChunk / 2; ++j) {
+                p[j] = ex2_approx(fmaf(__uint_as_float(v[j]), P.scale_log2, neg_m));
+                sum += p[j];
+              }
             }
             l = l * alpha + sum;
             if (owner) alpha_sh[srow_c] = alpha;
