@@ -51,7 +51,10 @@ constexpr int kMaxSlots = 4;
 constexpr int kSBufs = 2;                          // S accumulators (64 TMEM columns each)
 constexpr int kPTBytes = 64 * 128;                 // one P^T buffer: 64 rows x 64 keys bf16
 constexpr int kMaxPT = 2;
-constexpr int kPrefetchPages = 4;                  // L2 prefetch distance, in pages
+#ifndef MLA_PREFETCH_PAGES
+#define MLA_PREFETCH_PAGES 4
+#endif
+constexpr int kPrefetchPages = MLA_PREFETCH_PAGES;  // L2 prefetch distance, in pages
 constexpr int kDynSmemMax = 232448 - 2048;         // opt-in limit minus static smem budget
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 128;                   // O^T blocks at 128 + 64 m
