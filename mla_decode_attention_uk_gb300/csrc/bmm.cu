@@ -54,6 +54,8 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tok0 = blockIdx.x * NT;
   const int m0 = blockIdx.y * 128;
@@ -195,7 +197,9 @@ cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((BT + NT - 1) / NT, Mtot / 128, H);
-  kern<<<grid, kBmmThreads, smem, st>>>(tw, tx, BT, H, K, Kx, q, hi, lo, status);
+  e = launch_pdl(kern, grid, dim3(kBmmThreads), smem, st, 1, tw, tx, BT, H, K, Kx, q, hi, lo,
+                 status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace mla {
 
@@ -32,6 +33,8 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
                const uint8_t* __restrict__ ws, const PlanHeader* __restrict__ header, int B,
                int T, int H, const __nv_bfloat16* __restrict__ qlo,
                __nv_bfloat16* __restrict__ olat, float* __restrict__ lse_out, float scale) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int TH = T * H;
   const int b = blockIdx.y;
   const int r = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
@@ -121,9 +124,10 @@ cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, c
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
                            cudaStream_t st) {
   dim3 grid((T * H + kRowsPerCta - 1) / kRowsPerCta, B);
-  combine_kernel<<<grid, kCombThreads, 0, st>>>(seq_nsplit, seq_slot,
-                                                static_cast<const uint8_t*>(ws), header, B, T, H,
-                                                qlo, olat, lse, scale);
+  cudaError_t e = launch_pdl(combine_kernel, grid, dim3(kCombThreads), 0, st, 1, seq_nsplit,
+                             seq_slot, static_cast<const uint8_t*>(ws), header, B, T, H, qlo, olat,
+                             lse, scale);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -52,7 +52,7 @@ constexpr int kSBufs = 2;                          // S accumulators (64 TMEM co
 constexpr int kPTBytes = 64 * 128;                 // one P^T buffer: 64 rows x 64 keys bf16
 constexpr int kMaxPT = 2;
 #ifndef MLA_PREFETCH_PAGES
-#define MLA_PREFETCH_PAGES 4
+#define MLA_PREFETCH_PAGES 2
 #endif
 constexpr int kPrefetchPages = MLA_PREFETCH_PAGES;  // L2 prefetch distance, in pages
 constexpr int kDynSmemMax = 232448 - 2048;         // opt-in limit minus static smem budget
@@ -137,6 +137,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   __shared__ float alpha_sh[64];
   __shared__ float inv_l_sh[64];
 
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x % P.tiles;
   const int k0 = blockIdx.x / P.tiles;
@@ -645,19 +647,8 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
   P.scale = scale;
   P.scale_log2 = scale * 1.4426950408889634f;
 
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(groups * P.tiles, 1, 1);
-  cfg.blockDim = dim3(kDecThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = P.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = P.cluster > 1 ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, decode_kernel, tm_q, tm_c, P);
+  e = launch_pdl(decode_kernel, dim3(groups * P.tiles), dim3(kDecThreads), smem, st, P.cluster,
+                 tm_q, tm_c, P);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -89,6 +89,18 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, i
   return true;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Kernels of one decode step are launched with programmatic stream
+// serialisation: a kernel may start while its predecessor in the stream is
+// still running, so every kernel waits for the predecessor's completion (and
+// memory) before touching global memory, then lets its own successor launch.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
