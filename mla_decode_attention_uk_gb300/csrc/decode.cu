@@ -29,8 +29,8 @@
 //     double-buffered when the query tile is small enough to leave room.
 //   * Epilogue (warps 4-7): O / l to bf16 o_lat plus lse for unsplit sequences,
 //     or fp32 partials for split ones.
-// Warp roles: 0 TMA producer, 1-2 QK^T issuers (even / odd pages; warp 2 also
-// owns TMEM), 3 PV issuer, 4-7 softmax and epilogue.  The issuers work from precomputed descriptors so one
+// Warp roles: 0 TMA producer, 1-2 QK^T issuers (K halves; warp 2 also owns
+// TMEM), 3 and 8 PV issuers (latent halves), 4-7 softmax and epilogue.  The issuers work from precomputed descriptors so one
 // MMA costs an add and the issue itself.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -43,12 +43,12 @@ namespace mla {
 
 namespace {
 
-constexpr int kDecThreads = 256;
+constexpr int kDecThreads = 288;                   // 9 warps
 constexpr int kChunk = 64;                         // keys per streamed chunk (one page)
 constexpr int kChunkBox = kChunk * 128;            // one 64 x 64 bf16 box: 8 KB
 constexpr int kSlotBytes = kBoxes * kChunkBox;     // 72 KB
 constexpr int kMaxSlots = 4;
-constexpr int kSBufs = 2;                          // S accumulators (64 TMEM columns each)
+constexpr int kSBufs = 2;                          // S buffers, each two 64-column K halves
 constexpr int kPTBytes = 64 * 128;                 // one P^T buffer: 64 rows x 64 keys bf16
 constexpr int kMaxPT = 2;
 #ifndef MLA_PREFETCH_PAGES
@@ -57,7 +57,7 @@ constexpr int kMaxPT = 2;
 constexpr int kPrefetchPages = MLA_PREFETCH_PAGES;  // L2 prefetch distance, in pages
 constexpr int kDynSmemMax = 232448 - 2048;         // opt-in limit minus static smem budget
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 128;                   // O^T blocks at 128 + 64 m
+constexpr uint32_t kTmemO = 256;                   // O^T blocks at 256 + 64 m
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -131,7 +131,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, q_free, slot_full[kMaxSlots], slot_empty[kMaxSlots],
       s_full[kSBufs], s_free[kSBufs], p_full[kMaxPT], p_free[kMaxPT], o_full, o_free,
-      drain_bar[3];
+      drain_bar[4];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ float alpha_sh[64];
@@ -168,19 +168,19 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(smem_u32(&q_free), 2);
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&slot_full[i]), 1);
-      mbar_init(smem_u32(&slot_empty[i]), CS);
+      mbar_init(smem_u32(&slot_empty[i]), 2 * CS);
     }
     for (int i = 0; i < kSBufs; ++i) {
-      mbar_init(smem_u32(&s_full[i]), 1);
+      mbar_init(smem_u32(&s_full[i]), 2);
       mbar_init(smem_u32(&s_free[i]), 4);
     }
     for (int i = 0; i < NPT; ++i) {
       mbar_init(smem_u32(&p_full[i]), 4);
-      mbar_init(smem_u32(&p_free[i]), 1);
+      mbar_init(smem_u32(&p_free[i]), 2);
     }
-    mbar_init(smem_u32(&o_full), 1);
+    mbar_init(smem_u32(&o_full), 2);
     mbar_init(smem_u32(&o_free), 4);
-    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&drain_bar[i]), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&drain_bar[i]), 1);
     abort_sh = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -258,12 +258,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
     }
   }
-  if (warp >= 1 && warp <= 3) {
+  if ((warp >= 1 && warp <= 3) || warp == 8) {
     // ------------------------------------------------------------ MMA issuers
-    // Warps 1 and 2 issue QK^T for even and odd pages (a single issuing
-    // thread cannot keep the tensor pipe busy with M = 64 MMAs; two overlap),
-    // warp 3 issues PV as soon as the softmax has written P.  Each issuer
-    // commits its own MMAs.
+    // One issuing thread cannot keep the tensor pipe busy (each MMA costs it
+    // ~50 cycles), so every page's MMAs are spread over four issuers whose
+    // MMAs overlap: warps 1 and 2 issue the two K halves of QK^T into two
+    // accumulators (the softmax adds them), warps 3 and 8 issue PV for latent
+    // blocks 0-1 and 2-3 as soon as the softmax has written P.  Each issuer
+    // commits its own MMAs, so the barriers they signal count two arrivals.
     if (elect_one()) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(64, kChunk, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 64, true, false);
@@ -274,8 +276,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const uint64_t dpv0 = sdesc_sw128(sSlot0, kChunkBox, 1024);
       const uint64_t dpt0 = sdesc_sw128(sPT, 16, 1024);
       const uint32_t qbox16 = q_box_bytes >> 4;
-      const bool is_qk = warp != 3;
-      const int qk_par = warp - 1;  // page parity handled by this QK issuer
+      const bool is_qk = warp == 1 || warp == 2;
+      const int half = (warp == 1 || warp == 3) ? 0 : 1;  // K half (QK) / latent half (PV)
+      const int j0 = half == 0 ? 0 : 5, j1 = half == 0 ? 5 : kBoxes;  // QK boxes
       int g = 0, pc = 0;
       bool ok = true;
       for (int k = k0; k < R && ok; k += G) {
@@ -287,7 +290,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           if (is_qk) {
             if (!mbar_wait(smem_u32(&q_full), pc & 1, &abort_sh, P.status)) { ok = false; break; }
             for (int i = 0; i < nc; ++i, ++g) {
-              if ((g & 1) != qk_par) continue;
               const int s = g % NS, sb = g % kSBufs;
               if (!mbar_wait(smem_u32(&slot_full[s]), (g / NS) & 1, &abort_sh, P.status) ||
                   (g >= kSBufs && !mbar_wait(smem_u32(&s_free[sb]), ((g / kSBufs) - 1) & 1,
@@ -297,12 +299,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               }
               tc_fence_after();
               const uint64_t bd0 = dslot0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
-#pragma unroll
-              for (int j = 0; j < kBoxes; ++j) {
+              const uint32_t d = tmem + 128 * sb + 64 * half;
+              for (int j = j0; j < j1; ++j) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                  umma_bf16(tmem + kChunk * sb, dq0 + (j * qbox16 + kk * 2),
-                            bd0 + ((j * kChunkBox) >> 4) + kk * 2, idesc_qk, (j | kk) != 0);
+                  umma_bf16(d, dq0 + (j * qbox16 + kk * 2), bd0 + ((j * kChunkBox) >> 4) + kk * 2,
+                            idesc_qk, (j != j0) || (kk != 0));
                 }
               }
               umma_commit(smem_u32(&s_full[sb]));
@@ -326,7 +328,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               const uint64_t ad0 = dpv0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
               const uint64_t bd0 = dpt0 + static_cast<uint64_t>((pb2 * kPTBytes) >> 4);
 #pragma unroll
-              for (int m = 0; m < 4; ++m) {
+              for (int m = 2 * half; m < 2 * half + 2; ++m) {
 #pragma unroll
                 for (int kk = 0; kk < kChunk / 16; ++kk) {
                   umma_bf16(tmem + kTmemO + 64 * m, ad0 + ((2 * m * kChunkBox + kk * 2048) >> 4),
@@ -347,11 +349,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
       }
       // Drain this issuer's MMAs before TMEM is released.
-      const uint32_t db = smem_u32(&drain_bar[warp - 1]);
+      const uint32_t db = smem_u32(&drain_bar[warp == 8 ? 3 : warp - 1]);
       umma_commit(db);
       mbar_wait_drain(db, 0, P.status);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax + epilogue
     const int wq = warp - 4;                    // TMEM lane quarter
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
@@ -382,8 +384,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           uint32_t v[kChunk / 2];
           if (!bad) {
             tc_fence_after();
-            tmem_ld_16x64b_x32(tmem + lane_off + kChunk * sb, v);
+            uint32_t v2[kChunk / 2];
+            tmem_ld_16x64b_x32(tmem + lane_off + 128 * sb, v);
+            tmem_ld_16x64b_x32(tmem + lane_off + 128 * sb + 64, v2);
             tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < kChunk / 2; ++j)
+              v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v2[j]));
           }
           tc_fence_before();
           __syncwarp();
