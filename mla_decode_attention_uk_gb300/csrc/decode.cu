@@ -229,19 +229,24 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             return pg;
           };
-          auto prefetch = [&](int i) {
-            const int row = page_of(i) * kPage;
-            for (int j = crank; j < kBoxes; j += CS) tma_prefetch_l2_2d(&tm_c, j * kBoxCols, row);
-          };
-          for (int i = 0; i < cr.nchunks && i < kPrefetchPages; ++i) prefetch(i);
+          // Block-table entries are read kLookAhead pages early so the
+          // dependent global load stays off the slot-refill path.
+          constexpr int kLookAhead = kPrefetchPages > 0 ? kPrefetchPages : 1;
+          int ahead[kLookAhead];
+#pragma unroll
+          for (int a = 0; a < kLookAhead; ++a) {
+            ahead[a] = a < cr.nchunks ? page_of(a) : 0;
+            if (kPrefetchPages > 0 && a < cr.nchunks)
+              for (int j = crank; j < kBoxes; j += CS)
+                tma_prefetch_l2_2d(&tm_c, j * kBoxCols, ahead[a] * kPage);
+          }
           for (int i = 0; i < cr.nchunks; ++i, ++g) {
             const int s = g % NS, u = g / NS;
             if (u > 0 && !mbar_wait(smem_u32(&slot_empty[s]), (u - 1) & 1, &abort_sh, P.status)) {
               ok = false;
               break;
             }
-            if (i + kPrefetchPages < cr.nchunks) prefetch(i + kPrefetchPages);
-            const int row = page_of(i) * kPage;
+            const int row = ahead[0] * kPage;
             const uint32_t dst = sSlot0 + s * kSlotBytes;
             const uint32_t fb = smem_u32(&slot_full[s]);
             mbar_expect_tx(fb, kSlotBytes);
@@ -252,6 +257,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               for (int j = crank; j < kBoxes; j += CS)
                 tma_load_2d_mc(dst + j * kChunkBox, &tm_c, j * kBoxCols, row, fb, cmask);
             }
+            // Shift the look-ahead window and fetch (and L2-prefetch) the page
+            // kLookAhead chunks ahead.
+#pragma unroll
+            for (int a = 0; a + 1 < kLookAhead; ++a) ahead[a] = ahead[a + 1];
+            const int nxt = i + kLookAhead;
+            ahead[kLookAhead - 1] = nxt < cr.nchunks ? page_of(nxt) : 0;
+            if (kPrefetchPages > 0 && nxt < cr.nchunks)
+              for (int j = crank; j < kBoxes; j += CS)
+                tma_prefetch_l2_2d(&tm_c, j * kBoxCols, ahead[kLookAhead - 1] * kPage);
           }
           ++pc;
         }
@@ -399,17 +413,19 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const int kb = cr.key0(i) + par;    // key of v[0]; v[j] is key kb + 2 j
             // Max over raw scores (scale > 0), masking only on a sequence's
             // last page; then p = 2^(s * scale * log2 e - m) with one FFMA.
-            float vmax = -INFINITY;
-            if (kb + 2 * (kChunk / 2 - 1) < n_row) {
+            if (kb + 2 * (kChunk / 2 - 1) >= n_row) {
 #pragma unroll
-              for (int j = 0; j < kChunk / 2; ++j) vmax = fmaxf(vmax, __uint_as_float(v[j]));
-            } else {
-#pragma unroll
-              for (int j = 0; j < kChunk / 2; ++j) {
+              for (int j = 0; j < kChunk / 2; ++j)
                 if (kb + 2 * j >= n_row) v[j] = __float_as_uint(-INFINITY);
-                vmax = fmaxf(vmax, __uint_as_float(v[j]));
-              }
             }
+            // Tree reduction (independent partial maxima).
+            float mx[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) mx[q] = __uint_as_float(v[q]);
+#pragma unroll
+            for (int j = 8; j < kChunk / 2; ++j) mx[j & 7] = fmaxf(mx[j & 7], __uint_as_float(v[j]));
+            float vmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
             const float pmax = vmax * P.scale_log2;
             float alpha = 1.0f;
@@ -425,11 +441,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               for (int j = 0; j < kChunk / 2; ++j) p[j] = 0.0f;
             } else {
               const float neg_m = -m_used;
+              float sm[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
               for (int j = 0; j < kChunk / 2; ++j) {
                 p[j] = ex2_approx(fmaf(__uint_as_float(v[j]), P.scale_log2, neg_m));
-                sum += p[j];
+                sm[j & 3] += p[j];
               }
+              sum = (sm[0] + sm[1]) + (sm[2] + sm[3]);
             }
             l = l * alpha + sum;
             if (owner) alpha_sh[srow_c] = alpha;
