@@ -528,7 +528,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int m = 0; m < 4; ++m) {
           const int lat = 128 * m + 32 * wq + lane;
 #pragma unroll 1
-          for (int h2 = 0; h2 < 2; ++h2) {
+          for (int h2 = 0; h2 < 2 && 32 * h2 < rows_here; ++h2) {  // skip empty row halves
             uint32_t v[32];
             tmem_ld_x32(tmem + lane_off + kTmemO + 64 * m + 32 * h2, v);
             tmem_wait_ld();
