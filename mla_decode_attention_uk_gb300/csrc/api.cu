@@ -29,9 +29,9 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
                           const int32_t* block_table, const int32_t* seq_len_eff,
                           const PlanHeader* header, void* ws, const int32_t* seq_first,
                           const int32_t* seq_nsplit, const int32_t* seq_slot,
-                          const __nv_bfloat16* qlat, const __nv_bfloat16* qlo,
-                          __nv_bfloat16* olat, float* lse, int32_t* status, int B, int T, int H,
-                          int max_pages, int num_pages, float scale, cudaStream_t st);
+                          const __nv_bfloat16* qlo, __nv_bfloat16* olat, float* lse,
+                          int32_t* status, int B, int T, int H, int max_pages,
+                          int num_pages, float scale, cudaStream_t st);
 cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, const void* ws,
                            const PlanHeader* header, const __nv_bfloat16* qlo,
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
@@ -286,8 +286,7 @@ int mla_decode_attend(const mla_decode_dims* d, const void* kv_cache, const int3
   return cuda_rc(launch_decode(
       tm_q, tm_c, groups, block_table, at<int32_t>(ws, L.seq_len_eff), at<PlanHeader>(ws, L.header),
       ws, at<int32_t>(ws, L.seq_first), at<int32_t>(ws, L.seq_nsplit), at<int32_t>(ws, L.seq_slot),
-      at<__nv_bfloat16>(ws, L.qlat), at<__nv_bfloat16>(ws, L.qlo), at<__nv_bfloat16>(ws, L.olat),
-      lse,
+      at<__nv_bfloat16>(ws, L.qlo), at<__nv_bfloat16>(ws, L.olat), lse,
       at<int32_t>(ws, L.status), d->batch, d->q_len, d->num_heads, d->max_pages_per_seq,
       d->num_pages, scale, static_cast<cudaStream_t>(stream)));
 }

@@ -71,7 +71,6 @@ struct DecodeParams {
   const int32_t* seq_first;
   const int32_t* seq_nsplit;
   const int32_t* seq_slot;
-  const __nv_bfloat16* qlat; // [B*T*H, 576]  (read directly when the query tile lives in TMEM)
   const __nv_bfloat16* qlo;  // [B*T*H, 512]
   __nv_bfloat16* olat;       // [B*T*H, 512]
   float* lse;                // [B*T*H]
@@ -126,20 +125,9 @@ struct ChunkRange {
   __device__ int key0(int i) const { return (pbeg + i) * kPage; }
 };
 
-// QT (query in TMEM) specialisation, for at most 16 query rows per sequence:
-// the absorbed query tile is the A operand of QK^T read from TMEM (288
-// columns), PV runs with N = 16 rows (O^T needs 64 columns), and the shared
-// memory that the query tile and wide P^T buffers would take holds a third page
-// slot.
-template <bool QT>
 __global__ void __launch_bounds__(kDecThreads, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
               DecodeParams P) {
-  constexpr uint32_t kSCols = QT ? 64u : 128u;     // TMEM columns per S buffer
-  constexpr uint32_t kOCol = QT ? 128u : kTmemO;   // O^T base column
-  constexpr uint32_t kQCol = 192u;                 // query tile (QT only): 288 columns
-  constexpr int kPVN = QT ? 16 : 64;               // PV N = query rows per tile
-  constexpr int kPTB = kPVN * 128;                 // bytes per P^T buffer
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full, q_free, slot_full[kMaxSlots], slot_empty[kMaxSlots],
       s_full[kSBufs], s_free[kSBufs], p_full[kMaxPT], p_free[kMaxPT], o_full, o_free,
@@ -172,7 +160,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const uint32_t q_box_bytes = static_cast<uint32_t>(P.q_box_rows) * 128u;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = sbase;
-  const uint32_t sSlot0 = QT ? sbase : sQ + kBoxes * q_box_bytes;
+  const uint32_t sSlot0 = sQ + kBoxes * q_box_bytes;
   const uint32_t sPT = sSlot0 + NS * kSlotBytes;
 
   if (threadIdx.x == 0) {
@@ -183,7 +171,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(smem_u32(&slot_empty[i]), 2 * CS);
     }
     for (int i = 0; i < kSBufs; ++i) {
-      mbar_init(smem_u32(&s_full[i]), QT ? 1 : 2);
+      mbar_init(smem_u32(&s_full[i]), 2);
       mbar_init(smem_u32(&s_free[i]), 4);
     }
     for (int i = 0; i < NPT; ++i) {
@@ -214,22 +202,21 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     // ------------------------------------------------------------ TMA producer
     if (elect_one()) {
       const uint32_t q_bytes = q_box_bytes * kBoxes;
-      int g = 0, pc = 0;
+      int g = 0, pc = 0, nq = 0;  // nq: query-tile copies issued
       bool ok = true;
       for (int k = k0; k < R && ok; k += G) {
         PieceWalker w(P, k);
         int b, pb, pe;
         while (ok && w.next(P, b, pb, pe)) {
-          if (!QT) {
-            if (pc > 0 && !mbar_wait(smem_u32(&q_free), (pc - 1) & 1, &abort_sh, P.status)) {
-              ok = false;
-              break;
-            }
-            const int qrow = b * TH + tile * kTileRows;
-            mbar_expect_tx(smem_u32(&q_full), q_bytes);
-            for (int j = 0; j < kBoxes; ++j)
-              tma_load_2d(sQ + j * q_box_bytes, &tm_q, j * kBoxCols, qrow, smem_u32(&q_full));
+          if (pc > 0 && !mbar_wait(smem_u32(&q_free), (pc - 1) & 1, &abort_sh, P.status)) {
+            ok = false;
+            break;
           }
+          const int qrow = b * TH + tile * kTileRows;
+          mbar_expect_tx(smem_u32(&q_full), q_bytes);
+          for (int j = 0; j < kBoxes; ++j)
+            tma_load_2d(sQ + j * q_box_bytes, &tm_q, j * kBoxCols, qrow, smem_u32(&q_full));
+          ++nq;
           const ChunkRange cr(P.seq_len_eff[b], pb, pe);
           const int32_t* bt_row = P.block_table + static_cast<size_t>(b) * P.max_pages;
           // Pages are also prefetched into L2 kPrefetchPages ahead of their
@@ -284,6 +271,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           ++pc;
         }
       }
+      // After an abort the consumers may not have waited for every copy this
+      // thread started; wait (bounded) for the last query tile and the last
+      // page copy into each slot so that no copy lands after the CTA has exited.
+      if (nq > 0) mbar_wait_drain(smem_u32(&q_full), (nq - 1) & 1, P.status);
+      for (int s = 0; s < NS; ++s) {
+        const int n = (g - s + NS - 1) / NS;  // copies issued into slot s
+        if (n > 0) mbar_wait_drain(smem_u32(&slot_full[s]), (n - 1) & 1, P.status);
+      }
     }
   }
   if ((warp >= 1 && warp <= 3) || warp == 8) {
@@ -296,7 +291,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     // commits its own MMAs, so the barriers they signal count two arrivals.
     if (elect_one()) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(64, kChunk, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kPVN, true, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 64, true, false);
       // Descriptors differ only in the start-address field (bits 0-13, in
       // 16-byte units), so each MMA adds a small constant to a base.
       const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
@@ -318,8 +313,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           if (is_qk) {
             if (!mbar_wait(smem_u32(&q_full), pc & 1, &abort_sh, P.status)) { ok = false; break; }
             for (int i = 0; i < nc; ++i, ++g) {
-              // QT: one issuer per page (even / odd), full K, A from TMEM.
-              if (QT && (g & 1) != half) continue;
               const int s = g % NS, sb = g % kSBufs;
               if (!mbar_wait(smem_u32(&slot_full[s]), (g / NS) & 1, &abort_sh, P.status) ||
                   (g >= kSBufs && !mbar_wait(smem_u32(&s_free[sb]), ((g / kSBufs) - 1) & 1,
@@ -329,24 +322,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               }
               tc_fence_after();
               const uint64_t bd0 = dslot0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
-              if (QT) {
-                const uint32_t d = tmem + kSCols * sb;
+              const uint32_t d = tmem + 128 * sb + 64 * half;
+              for (int j = j0; j < j1; ++j) {
 #pragma unroll
-                for (int j = 0; j < kBoxes; ++j) {
-#pragma unroll
-                  for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16_ts(d, tmem + kQCol + 32 * j + 8 * kk,
-                                 bd0 + ((j * kChunkBox) >> 4) + kk * 2, idesc_qk, (j | kk) != 0);
-                }
-              } else {
-                const uint32_t d = tmem + kSCols * sb + 64 * half;
-                for (int j = j0; j < j1; ++j) {
-#pragma unroll
-                  for (int kk = 0; kk < 4; ++kk) {
-                    umma_bf16(d, dq0 + (j * qbox16 + kk * 2),
-                              bd0 + ((j * kChunkBox) >> 4) + kk * 2, idesc_qk,
-                              (j != j0) || (kk != 0));
-                  }
+                for (int kk = 0; kk < 4; ++kk) {
+                  umma_bf16(d, dq0 + (j * qbox16 + kk * 2), bd0 + ((j * kChunkBox) >> 4) + kk * 2,
+                            idesc_qk, (j != j0) || (kk != 0));
                 }
               }
               umma_commit(smem_u32(&s_full[sb]));
@@ -368,12 +349,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               tc_fence_after();
               const int s = g % NS;
               const uint64_t ad0 = dpv0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
-              const uint64_t bd0 = dpt0 + static_cast<uint64_t>((pb2 * kPTB) >> 4);
+              const uint64_t bd0 = dpt0 + static_cast<uint64_t>((pb2 * kPTBytes) >> 4);
 #pragma unroll
               for (int m = 2 * half; m < 2 * half + 2; ++m) {
 #pragma unroll
                 for (int kk = 0; kk < kChunk / 16; ++kk) {
-                  umma_bf16(tmem + kOCol + kPVN * m, ad0 + ((2 * m * kChunkBox + kk * 2048) >> 4),
+                  umma_bf16(tmem + kTmemO + 64 * m, ad0 + ((2 * m * kChunkBox + kk * 2048) >> 4),
                             bd0 + kk * 2, idesc_pv, !(first && kk == 0));
                 }
               }
@@ -416,37 +397,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int L = P.seq_len_eff[b];
         const int n_row = row_ok ? L - P.T + r / P.H + 1 : 0;
         float m_used = -INFINITY, l = 0.0f;     // l: this thread's half of the row sum
-        if (QT && wq == 0) {
-          // Load this piece's query rows into TMEM (A operand of QK^T): lane L
-          // holds row L; each 32-bit column packs two consecutive bf16 of K,
-          // which is the row's order in memory.  Waits until the previous
-          // piece's QK^T MMAs are done reading the tile.
-          bool qbad = pc > 0 && !mbar_wait(smem_u32(&q_free), (pc - 1) & 1, &abort_sh, P.status);
-          qbad = __any_sync(0xffffffffu, qbad);
-          if (!qbad) {
-            const bool qrow_ok = lane < 16 && lane < TH;
-            const uint4* src = reinterpret_cast<const uint4*>(
-                P.qlat + (static_cast<size_t>(b) * TH + (qrow_ok ? lane : 0)) * kDqk);
-            tc_fence_after();
-#pragma unroll 1
-            for (int cch = 0; cch < kDqk / 64; ++cch) {
-              uint32_t words[32];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const uint4 x = qrow_ok ? __ldg(src + cch * 8 + u) : make_uint4(0, 0, 0, 0);
-                words[4 * u] = x.x;
-                words[4 * u + 1] = x.y;
-                words[4 * u + 2] = x.z;
-                words[4 * u + 3] = x.w;
-              }
-              tmem_st_x32(tmem + lane_off + kQCol + 32 * cch, words);
-            }
-            tmem_wait_st();
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&q_full));
-        }
         const ChunkRange cr(L, pb, pe);
         const int nc = cr.nchunks;
         for (int i = 0; i < nc; ++i, ++g) {
@@ -457,17 +407,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           uint32_t v[kChunk / 2];
           if (!bad) {
             tc_fence_after();
-            tmem_ld_16x64b_x32(tmem + lane_off + kSCols * sb, v);
-            if (!QT) {
-              uint32_t v2[kChunk / 2];
-              tmem_ld_16x64b_x32(tmem + lane_off + kSCols * sb + 64, v2);
-              tmem_wait_ld();
+            uint32_t v2[kChunk / 2];
+            tmem_ld_16x64b_x32(tmem + lane_off + 128 * sb, v);
+            tmem_ld_16x64b_x32(tmem + lane_off + 128 * sb + 64, v2);
+            tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < kChunk / 2; ++j)
-                v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v2[j]));
-            } else {
-              tmem_wait_ld();
-            }
+            for (int j = 0; j < kChunk / 2; ++j)
+              v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v2[j]));
           }
           tc_fence_before();
           __syncwarp();
@@ -528,8 +474,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (g >= NPT && !mbar_wait(smem_u32(&p_free[pb2]), ((g / NPT) - 1) & 1, &abort_sh,
                                        P.status))
               bad = true;
-            if (!bad && srow_c < kPVN) {
-              const uint32_t rowaddr = sPT + pb2 * kPTB + srow_c * 128;
+            if (!bad) {
+              const uint32_t rowaddr = sPT + pb2 * kPTBytes + srow_c * 128;
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 const int lchunk = 4 * par + q;
@@ -552,27 +498,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tc_fence_after();
 #pragma unroll 1
             for (int m = 0; m < 4; ++m) {
-              if (QT) {
-                uint32_t vv[16];
-                const uint32_t ta = tmem + lane_off + kOCol + kPVN * m;
-                tmem_ld_x16(ta, reinterpret_cast<uint32_t(&)[16]>(vv));
+#pragma unroll 1
+              for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t vv[32];
+                const uint32_t ta = tmem + lane_off + kTmemO + 64 * m + 32 * h2;
+                tmem_ld_x32(ta, vv);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  vv[j] = __float_as_uint(__uint_as_float(vv[j]) * alpha_sh[j]);
-                tmem_st_x16(ta, vv);
-              } else {
-#pragma unroll 1
-                for (int h2 = 0; h2 < 2; ++h2) {
-                  uint32_t vv[32];
-                  const uint32_t ta = tmem + lane_off + kOCol + 64 * m + 32 * h2;
-                  tmem_ld_x32(ta, vv);
-                  tmem_wait_ld();
-#pragma unroll
-                  for (int j = 0; j < 32; ++j)
-                    vv[j] = __float_as_uint(__uint_as_float(vv[j]) * alpha_sh[32 * h2 + j]);
-                  tmem_st_x32(ta, vv);
-                }
+                for (int j = 0; j < 32; ++j)
+                  vv[j] = __float_as_uint(__uint_as_float(vv[j]) * alpha_sh[32 * h2 + j]);
+                tmem_st_x32(ta, vv);
               }
             }
             tmem_wait_st();
@@ -601,26 +536,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll 1
         for (int m = 0; m < 4; ++m) {
           const int lat = 128 * m + 32 * wq + lane;
-          if (QT) {
-            uint32_t v[16];
-            tmem_ld_x16(tmem + lane_off + kOCol + kPVN * m, reinterpret_cast<uint32_t(&)[16]>(v));
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (j < rows_here) {
-                const float val = __uint_as_float(v[j]) * inv_l_sh[j];
-                if (nsplit > 1)
-                  opart[(part_base + j) * kLora + lat] = val;
-                else
-                  olat[(row_base + j) * kLora + lat] = __float2bfloat16_rn(val);
-              }
-            }
-            continue;
-          }
 #pragma unroll 1
           for (int h2 = 0; h2 < 2 && 32 * h2 < rows_here; ++h2) {  // skip empty row halves
             uint32_t v[32];
-            tmem_ld_x32(tmem + lane_off + kOCol + 64 * m + 32 * h2, v);
+            tmem_ld_x32(tmem + lane_off + kTmemO + 64 * m + 32 * h2, v);
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -671,24 +590,18 @@ int decode_q_box_rows(int T, int H) {
   const int r = T * H;
   return r >= kTileRows ? kTileRows : ((r + 7) / 8) * 8;
 }
-// Query tile in TMEM (and PV with N = 16) for at most 16 query rows.
-bool decode_qt(int T, int H) { return T * H <= 16; }
 // Page slots and P^T buffers that fit next to the query tile: two P^T
-// buffers when two page slots still fit, else one.  With the query tile in
-// TMEM three page slots and two 2 KB P^T buffers fit.
+// buffers when two page slots still fit, else one.
 int decode_num_pt(int T, int H) {
-  if (decode_qt(T, H)) return 2;
   const int q_bytes = kBoxes * decode_q_box_rows(T, H) * 128;
   return (kDynSmemMax - 1024 - q_bytes - 2 * kPTBytes) / kSlotBytes >= 2 ? 2 : 1;
 }
 int decode_num_slots(int T, int H) {
-  if (decode_qt(T, H)) return 3;
   const int q_bytes = kBoxes * decode_q_box_rows(T, H) * 128;
   int ns = (kDynSmemMax - 1024 - q_bytes - decode_num_pt(T, H) * kPTBytes) / kSlotBytes;
   return ns > kMaxSlots ? kMaxSlots : ns;
 }
 int decode_smem_bytes(int T, int H) {
-  if (decode_qt(T, H)) return 1024 + decode_num_slots(T, H) * kSlotBytes + 2 * 16 * 128;
   return 1024 + kBoxes * decode_q_box_rows(T, H) * 128 + decode_num_slots(T, H) * kSlotBytes +
          decode_num_pt(T, H) * kPTBytes;
 }
@@ -703,8 +616,8 @@ cudaError_t decode_max_groups(int T, int H, int sm_count, int* groups) {
   const int cs = decode_cluster_size(T, H);
   const int tiles = decode_tiles(T, H);
   const int smem = decode_smem_bytes(T, H);
-  auto kern = decode_qt(T, H) ? decode_kernel<true> : decode_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem);
   if (e != cudaSuccess) return e;
   if (cs == 1) {
     *groups = sm_count / tiles > 0 ? sm_count / tiles : 1;
@@ -722,7 +635,7 @@ cudaError_t decode_max_groups(int T, int H, int sm_count, int* groups) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, decode_kernel, &cfg);
   if (e != cudaSuccess) return e;
   *groups = n > 0 ? n : 1;
   return cudaSuccess;
@@ -732,12 +645,12 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
                           const int32_t* block_table, const int32_t* seq_len_eff,
                           const PlanHeader* header, void* ws, const int32_t* seq_first,
                           const int32_t* seq_nsplit, const int32_t* seq_slot,
-                          const __nv_bfloat16* qlat, const __nv_bfloat16* qlo,
-                          __nv_bfloat16* olat, float* lse, int32_t* status, int B, int T, int H,
-                          int max_pages, int num_pages, float scale, cudaStream_t st) {
+                          const __nv_bfloat16* qlo, __nv_bfloat16* olat, float* lse,
+                          int32_t* status, int B, int T, int H, int max_pages,
+                          int num_pages, float scale, cudaStream_t st) {
   const int smem = decode_smem_bytes(T, H);
-  auto kern = decode_qt(T, H) ? decode_kernel<true> : decode_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem);
   if (e != cudaSuccess) return e;
   DecodeParams P;
   P.block_table = block_table;
@@ -749,7 +662,6 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
   P.seq_first = seq_first;
   P.seq_nsplit = seq_nsplit;
   P.seq_slot = seq_slot;
-  P.qlat = qlat;
   P.qlo = qlo;
   P.olat = olat;
   P.lse = lse;
@@ -769,8 +681,8 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
   P.scale = scale;
   P.scale_log2 = scale * 1.4426950408889634f;
 
-  e = launch_pdl(kern, dim3(groups * P.tiles), dim3(kDecThreads), smem, st, P.cluster, tm_q, tm_c,
-                 P);
+  e = launch_pdl(decode_kernel, dim3(groups * P.tiles), dim3(kDecThreads), smem, st, P.cluster,
+                 tm_q, tm_c, P);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -126,6 +126,45 @@ def test_seq_len_beyond_block_table_sets_status():
     assert m.check() == 5
 
 
+def _late_pages_score_higher(inp, step, seed=0):
+    """Add (page index in the sequence) * step * u to every key's k_pe columns,
+    u one fixed random direction.  For a row whose q_pe has a positive
+    component along u, later pages then score higher as a whole: the running
+    max grows page after page and the online softmax must rescale its
+    accumulator, while scores within a page keep their spread (the attention
+    stays spread over many keys, so outputs stay O(1)).  Latent (value)
+    columns are untouched."""
+    g = torch.Generator().manual_seed(seed)
+    u = torch.randn(64, generator=g, dtype=torch.float64) / 8.0
+    cache = inp.cache.clone()
+    for b in range(inp.block_table.shape[0]):
+        n = (int(inp.seq_lens[b]) + 63) // 64
+        for i in range(n):
+            pg = int(inp.block_table[b, i])
+            cache[pg, :, 512:] = (cache[pg, :, 512:].double() + step * i * u).to(torch.bfloat16)
+    inp.cache = cache
+    return inp
+
+
+@pytest.mark.parametrize("H,T,R", [(16, 1, 1), (16, 1, 3), (16, 2, 1), (32, 1, 2), (64, 1, 1),
+                                   (128, 1, 3), (128, 2, 1)])
+def test_late_pages_force_rescale(H, T, R):
+    lens = [700, 2500, 130]
+    inp = _late_pages_score_higher(make_inputs(len(lens), lens, T, H, seed=300 + H + T), 8.0)
+    # The case needs rescales: for some row of sequence 1 a late page's LSE
+    # exceeds the first page's by more than the 8-bit (log2) rescale threshold
+    # plus ln 64 (the most a page's LSE can exceed its max score).
+    need = 0
+    for h in range(H):
+        args = (inp.q, inp.cache, inp.block_table, inp.seq_lens, inp.w_uk, inp.scale, 1, 0, h)
+        _, l_first = oracle.partial(*args, 0, 64)
+        _, l_late = oracle.partial(*args, 2432, 2496)
+        need += l_late - l_first > 8 * math.log(2) + math.log(64)
+    assert need >= max(1, H // 8)
+    out, lse, _ = run_gpu(inp, num_ranges=R)
+    assert_parity(compare(inp, out, lse), "H=%d T=%d R=%d" % (H, T, R))
+
+
 @pytest.mark.parametrize("name", ["tp_shard", "full_head", "long", "mixed_spec"])
 def test_full_size_workloads_sampled(name):
     inp = workload_inputs(name)
