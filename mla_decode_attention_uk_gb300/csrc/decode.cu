@@ -531,26 +531,32 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const size_t part_base =
             nsplit > 1 ? (static_cast<size_t>(P.seq_slot[b] + split) * TH + tile * kTileRows) : 0;
         const int rows_here = min(kTileRows, TH - tile * kTileRows);
-        __nv_bfloat16* __restrict__ olat = P.olat;
-        float* __restrict__ opart = P.opart;
+        // Row halves outer, latent blocks inner: each thread keeps the 32
+        // reciprocals of its half in registers, so the stores (one row each,
+        // coalesced over the warp's 32 latent columns) do not wait on
+        // shared-memory loads.
 #pragma unroll 1
-        for (int m = 0; m < 4; ++m) {
-          const int lat = 128 * m + 32 * wq + lane;
+        for (int h2 = 0; h2 < 2 && 32 * h2 < rows_here; ++h2) {  // skip empty row halves
+          float il[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) il[j] = inv_l_sh[32 * h2 + j];
+          const int nrow = min(32, rows_here - 32 * h2);
 #pragma unroll 1
-          for (int h2 = 0; h2 < 2 && 32 * h2 < rows_here; ++h2) {  // skip empty row halves
+          for (int m = 0; m < 4; ++m) {
+            const int lat = 128 * m + 32 * wq + lane;
             uint32_t v[32];
             tmem_ld_x32(tmem + lane_off + kTmemO + 64 * m + 32 * h2, v);
             tmem_wait_ld();
+            if (nsplit > 1) {
+              float* dst = P.opart + (part_base + 32 * h2) * kLora + lat;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int cc = 32 * h2 + j;
-              if (cc < rows_here) {
-                const float val = __uint_as_float(v[j]) * inv_l_sh[cc];
-                if (nsplit > 1)
-                  opart[(part_base + cc) * kLora + lat] = val;
-                else
-                  olat[(row_base + cc) * kLora + lat] = __float2bfloat16_rn(val);
-              }
+              for (int j = 0; j < 32; ++j)
+                if (j < nrow) dst[j * kLora] = __uint_as_float(v[j]) * il[j];
+            } else {
+              __nv_bfloat16* dst = P.olat + (row_base + 32 * h2) * kLora + lat;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < nrow) dst[j * kLora] = __float2bfloat16_rn(__uint_as_float(v[j]) * il[j]);
             }
           }
         }
