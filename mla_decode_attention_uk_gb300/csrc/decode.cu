@@ -129,7 +129,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
               DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t q_full, q_free, slot_full[kMaxSlots], slot_empty[kMaxSlots],
+  // slot_full has one barrier per box, so QK^T can start on the first boxes of
+  // a page while the rest are still in flight.
+  __shared__ __align__(8) uint64_t q_full, q_free, slot_full[kMaxSlots][kBoxes], slot_empty[kMaxSlots],
       s_full[kSBufs], s_free[kSBufs], p_full[kMaxPT], p_free[kMaxPT], o_full, o_free,
       drain_bar[4];
   __shared__ uint32_t tmem_base_sh;
@@ -167,7 +169,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(smem_u32(&q_full), 1);
     mbar_init(smem_u32(&q_free), 2);
     for (int i = 0; i < NS; ++i) {
-      mbar_init(smem_u32(&slot_full[i]), 1);
+      for (int j = 0; j < kBoxes; ++j) mbar_init(smem_u32(&slot_full[i][j]), 1);
       mbar_init(smem_u32(&slot_empty[i]), 2 * CS);
     }
     for (int i = 0; i < kSBufs; ++i) {
@@ -175,7 +177,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(smem_u32(&s_free[i]), 4);
     }
     for (int i = 0; i < NPT; ++i) {
-      mbar_init(smem_u32(&p_full[i]), 4);
+      mbar_init(smem_u32(&p_full[i]), 1);
       mbar_init(smem_u32(&p_free[i]), 2);
     }
     mbar_init(smem_u32(&o_full), 2);
@@ -249,13 +251,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             const int row = ahead[0] * kPage;
             const uint32_t dst = sSlot0 + s * kSlotBytes;
-            const uint32_t fb = smem_u32(&slot_full[s]);
-            mbar_expect_tx(fb, kSlotBytes);
-            if (CS == 1) {
-              for (int j = 0; j < kBoxes; ++j)
+            // Boxes in the order the two QK^T issuers consume them (0-4 and
+            // 5-8 interleaved).  With a cluster each CTA loads every CS-th box
+            // and multicasts it; every CTA expects all nine on its own barriers.
+#pragma unroll 1
+            for (int t = 0; t < kBoxes; ++t) {
+              const int j = (t & 1) ? 5 + (t >> 1) : (t >> 1);
+              const uint32_t fb = smem_u32(&slot_full[s][j]);
+              mbar_expect_tx(fb, kChunkBox);
+              if (CS == 1)
                 tma_load_2d(dst + j * kChunkBox, &tm_c, j * kBoxCols, row, fb);
-            } else {
-              for (int j = crank; j < kBoxes; j += CS)
+              else if (j % CS == crank)
                 tma_load_2d_mc(dst + j * kChunkBox, &tm_c, j * kBoxCols, row, fb, cmask);
             }
             // Shift the look-ahead window and fetch (and L2-prefetch) the page
@@ -277,7 +283,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (nq > 0) mbar_wait_drain(smem_u32(&q_full), (nq - 1) & 1, P.status);
       for (int s = 0; s < NS; ++s) {
         const int n = (g - s + NS - 1) / NS;  // copies issued into slot s
-        if (n > 0) mbar_wait_drain(smem_u32(&slot_full[s]), (n - 1) & 1, P.status);
+        if (n > 0)
+          for (int j = 0; j < kBoxes; ++j)
+            mbar_wait_drain(smem_u32(&slot_full[s][j]), (n - 1) & 1, P.status);
       }
     }
   }
@@ -314,22 +322,27 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (!mbar_wait(smem_u32(&q_full), pc & 1, &abort_sh, P.status)) { ok = false; break; }
             for (int i = 0; i < nc; ++i, ++g) {
               const int s = g % NS, sb = g % kSBufs;
-              if (!mbar_wait(smem_u32(&slot_full[s]), (g / NS) & 1, &abort_sh, P.status) ||
-                  (g >= kSBufs && !mbar_wait(smem_u32(&s_free[sb]), ((g / kSBufs) - 1) & 1,
-                                             &abort_sh, P.status))) {
+              if (g >= kSBufs && !mbar_wait(smem_u32(&s_free[sb]), ((g / kSBufs) - 1) & 1,
+                                            &abort_sh, P.status)) {
                 ok = false;
                 break;
               }
-              tc_fence_after();
               const uint64_t bd0 = dslot0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
               const uint32_t d = tmem + 128 * sb + 64 * half;
-              for (int j = j0; j < j1; ++j) {
+              for (int j = j0; j < j1 && ok; ++j) {
+                // Each box's MMAs go out as soon as that box has landed.
+                if (!mbar_wait(smem_u32(&slot_full[s][j]), (g / NS) & 1, &abort_sh, P.status)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                   umma_bf16(d, dq0 + (j * qbox16 + kk * 2), bd0 + ((j * kChunkBox) >> 4) + kk * 2,
                             idesc_qk, (j != j0) || (kk != 0));
                 }
               }
+              if (!ok) break;
               umma_commit(smem_u32(&s_full[sb]));
             }
             if (!ok) break;
@@ -514,8 +527,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tc_fence_before();
             named_bar_sync(1, 128);  // alpha_sh is rewritten by the next chunk
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&p_full[g % NPT]));
+          // The barrier above ordered all four warps' P^T writes (and any
+          // rescale) before this point: one arrival releases the PV issuers.
+          if (threadIdx.x == 128) mbar_arrive(smem_u32(&p_full[g % NPT]));
         }
         if (fail) break;
 
