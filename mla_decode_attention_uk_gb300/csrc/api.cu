@@ -132,8 +132,8 @@ int check_dims(const mla_decode_dims* d) {
 }
 
 // Default number of work ranges = co-resident decode CTA groups (one group =
-// the CTAs covering all query rows of a sequence, a cluster when it has 2 or 4
-// CTAs).  Cached per device and (q_len, heads).
+// the CTAs covering all query rows of a sequence).  Cached per device and
+// (q_len, heads).
 int g_groups[kMaxDevices][3][9];
 std::mutex g_groups_mu;
 

@@ -197,7 +197,7 @@ cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((BT + NT - 1) / NT, Mtot / 128, H);
-  e = launch_pdl(kern, grid, dim3(kBmmThreads), smem, st, 1, tw, tx, BT, H, K, Kx, q, hi, lo,
+  e = launch_pdl(kern, grid, dim3(kBmmThreads), smem, st, tw, tx, BT, H, K, Kx, q, hi, lo,
                  status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

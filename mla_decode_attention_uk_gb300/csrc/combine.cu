@@ -124,7 +124,7 @@ cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, c
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
                            cudaStream_t st) {
   dim3 grid((T * H + kRowsPerCta - 1) / kRowsPerCta, B);
-  cudaError_t e = launch_pdl(combine_kernel, grid, dim3(kCombThreads), 0, st, 1, seq_nsplit,
+  cudaError_t e = launch_pdl(combine_kernel, grid, dim3(kCombThreads), 0, st, seq_nsplit,
                              seq_slot, static_cast<const uint8_t*>(ws), header, B, T, H, qlo, olat,
                              lse, scale);
   if (e != cudaSuccess) return e;

@@ -12,10 +12,11 @@
 // GB300 mapping (one CTA = 64 query rows of one sequence, one work range):
 //   * Keys stream page by page: the TMA producer gathers a 64-token page as 9
 //     boxes of 64 x 64 bf16 (128B swizzle) into a ring of 72 KB slots, looking
-//     the physical page up in the block table.  When the
-//     query rows of a sequence span 2 or 4 CTAs, those CTAs form a cluster and
-//     each loads a share of every chunk with TMA multicast, so a chunk leaves
-//     L2 once per cluster.
+//     the physical page up in the block table.  When the query rows of a
+//     sequence span 2 or 4 CTAs (tiles), those CTAs stream the same pages at
+//     about the same time and the second read of a page is served by L2; they
+//     are not coupled (a cluster sharing pages by multicast made every slot
+//     refill wait for the slower CTA, which cost more than it saved).
 //   * QK^T on tcgen05: S[row, key] = sum_576 Q[row] C[key]; M = 64 rows, N = 64
 //     keys, fp32 in TMEM (an M = 64 accumulator puts 16 rows in each 32-lane
 //     quarter), two S buffers.  A whole page per MMA keeps the shared-memory
@@ -77,7 +78,7 @@ struct DecodeParams {
   float* opart;              // [slots, T*H, 512]
   float* lpart;              // [slots, T*H]
   int32_t* status;
-  int B, T, H, max_pages, num_pages, tiles, q_box_rows, num_slots, num_pt, cluster;
+  int B, T, H, max_pages, num_pages, tiles, q_box_rows, num_slots, num_pt;
   float scale, scale_log2;
 };
 
@@ -149,9 +150,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int TH = P.T * P.H;
   const int NS = P.num_slots;
   const int NPT = P.num_pt;                       // P^T buffers (1 or 2)
-  const int CS = P.cluster;                       // CTAs sharing each chunk (1, 2 or 4)
-  const int crank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const uint16_t cmask = static_cast<uint16_t>((1u << CS) - 1u);
   {
     const WsLayout L = make_layout(P.B, P.T, P.H, R);
     P.range_b = reinterpret_cast<const int32_t*>(P.ws + L.range_b);
@@ -170,7 +168,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(smem_u32(&q_free), 2);
     for (int i = 0; i < NS; ++i) {
       for (int j = 0; j < kBoxes; ++j) mbar_init(smem_u32(&slot_full[i][j]), 1);
-      mbar_init(smem_u32(&slot_empty[i]), 2 * CS);
+      mbar_init(smem_u32(&slot_empty[i]), 2);
     }
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(smem_u32(&s_full[i]), 2);
@@ -194,9 +192,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   }
   tc_fence_before();
   __syncthreads();
-  // Peers multicast into this CTA's slots and arrive on its barriers: they
-  // must all be initialised first.
-  if (CS > 1) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
@@ -240,7 +235,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           for (int a = 0; a < kLookAhead; ++a) {
             ahead[a] = a < cr.nchunks ? page_of(a) : 0;
             if (kPrefetchPages > 0 && a < cr.nchunks)
-              for (int j = crank; j < kBoxes; j += CS)
+              for (int j = 0; j < kBoxes; ++j)
                 tma_prefetch_l2_2d(&tm_c, j * kBoxCols, ahead[a] * kPage);
           }
           for (int i = 0; i < cr.nchunks; ++i, ++g) {
@@ -252,17 +247,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const int row = ahead[0] * kPage;
             const uint32_t dst = sSlot0 + s * kSlotBytes;
             // Boxes in the order the two QK^T issuers consume them (0-4 and
-            // 5-8 interleaved).  With a cluster each CTA loads every CS-th box
-            // and multicasts it; every CTA expects all nine on its own barriers.
+            // 5-8 interleaved).
 #pragma unroll 1
             for (int t = 0; t < kBoxes; ++t) {
               const int j = (t & 1) ? 5 + (t >> 1) : (t >> 1);
               const uint32_t fb = smem_u32(&slot_full[s][j]);
               mbar_expect_tx(fb, kChunkBox);
-              if (CS == 1)
-                tma_load_2d(dst + j * kChunkBox, &tm_c, j * kBoxCols, row, fb);
-              else if (j % CS == crank)
-                tma_load_2d_mc(dst + j * kChunkBox, &tm_c, j * kBoxCols, row, fb, cmask);
+              tma_load_2d(dst + j * kChunkBox, &tm_c, j * kBoxCols, row, fb);
             }
             // Shift the look-ahead window and fetch (and L2-prefetch) the page
             // kLookAhead chunks ahead.
@@ -271,7 +262,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const int nxt = i + kLookAhead;
             ahead[kLookAhead - 1] = nxt < cr.nchunks ? page_of(nxt) : 0;
             if (kPrefetchPages > 0 && nxt < cr.nchunks)
-              for (int j = crank; j < kBoxes; j += CS)
+              for (int j = 0; j < kBoxes; ++j)
                 tma_prefetch_l2_2d(&tm_c, j * kBoxCols, ahead[kLookAhead - 1] * kPage);
           }
           ++pc;
@@ -372,10 +363,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
               }
               umma_commit(smem_u32(&p_free[pb2]));
-              if (CS == 1)
-                umma_commit(smem_u32(&slot_empty[s]));
-              else
-                umma_commit_mc(smem_u32(&slot_empty[s]), cmask);
+              umma_commit(smem_u32(&slot_empty[s]));
             }
             if (!ok) break;
             umma_commit(smem_u32(&o_full));
@@ -595,8 +583,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
-  // No peer may still arrive on this CTA's barriers once it exits.
-  if (CS > 1) cluster_sync_all();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -625,39 +611,14 @@ int decode_smem_bytes(int T, int H) {
   return 1024 + kBoxes * decode_q_box_rows(T, H) * 128 + decode_num_slots(T, H) * kSlotBytes +
          decode_num_pt(T, H) * kPTBytes;
 }
-// CTAs that share each key chunk through TMA multicast (a cluster).
-int decode_cluster_size(int T, int H) {
-  const int tiles = decode_tiles(T, H);
-  return (tiles == 2 || tiles == 4) ? tiles : 1;
-}
-
-// Largest number of co-resident CTA groups (clusters of decode_cluster_size).
+// Largest number of co-resident CTA groups (one CTA per tile of a sequence's
+// query rows; one CTA per SM).
 cudaError_t decode_max_groups(int T, int H, int sm_count, int* groups) {
-  const int cs = decode_cluster_size(T, H);
   const int tiles = decode_tiles(T, H);
-  const int smem = decode_smem_bytes(T, H);
   cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem);
+                                       decode_smem_bytes(T, H));
   if (e != cudaSuccess) return e;
-  if (cs == 1) {
-    *groups = sm_count / tiles > 0 ? sm_count / tiles : 1;
-    return cudaSuccess;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cs * (sm_count / cs), 1, 1);
-  cfg.blockDim = dim3(kDecThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, decode_kernel, &cfg);
-  if (e != cudaSuccess) return e;
-  *groups = n > 0 ? n : 1;
+  *groups = sm_count / tiles > 0 ? sm_count / tiles : 1;
   return cudaSuccess;
 }
 
@@ -697,11 +658,10 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
   P.q_box_rows = decode_q_box_rows(T, H);
   P.num_slots = decode_num_slots(T, H);
   P.num_pt = decode_num_pt(T, H);
-  P.cluster = decode_cluster_size(T, H);
   P.scale = scale;
   P.scale_log2 = scale * 1.4426950408889634f;
 
-  e = launch_pdl(decode_kernel, dim3(groups * P.tiles), dim3(kDecThreads), smem, st, P.cluster,
+  e = launch_pdl(decode_kernel, dim3(groups * P.tiles), dim3(kDecThreads), smem, st,
                  tm_q, tm_c, P);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

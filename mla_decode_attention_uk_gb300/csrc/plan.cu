@@ -138,7 +138,7 @@ cudaError_t launch_plan(const int32_t* seq_lens, int B, int T, int max_pages, in
                         int32_t* status, PlanHeader* header, int32_t* range_b, int32_t* range_p,
                         int32_t* seq_first, int32_t* seq_nsplit, int32_t* seq_slot,
                         int32_t* seq_len_eff, int32_t* prefix, cudaStream_t stream) {
-  cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, 1, seq_lens, B,
+  cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, seq_lens, B,
                              T, max_pages, R, status, header, range_b, range_p, seq_first,
                              seq_nsplit, seq_slot, seq_len_eff, prefix);
   if (e != cudaSuccess) return e;
