@@ -34,6 +34,7 @@ from mla_decode_attention_uk_gb300.inputs import WORKLOADS, workload_inputs  # n
 
 METRIC = "MLA decode latent-KV GB/s, TFLOPS & tokens/s vs GB300 roofline (1 GPU)"
 DEFAULT_WORKLOAD = "tp_shard"
+PER_GRAPH = 10  # decode steps captured in one CUDA graph replay
 BYTES_PER_TOKEN = 1152          # 576 bf16 per cached token
 FLOP_PER_ROW_KEY = 2 * (576 + 512)
 FLOP_PER_ROW_BMM = 2 * 2 * 128 * 512
@@ -293,9 +294,12 @@ def main():
     if st != 0:
         raise SystemExit("device status %d after warm-up" % st)
 
-    # The step is launch-bound on the host for small batches: capture it once
-    # in a CUDA graph and replay it (same kernels, same arguments).
-    graph_step = graph_attend = None
+    # The step is launch-bound on the host for small batches: capture
+    # PER_GRAPH consecutive steps in one CUDA graph and replay it (same
+    # kernels, same arguments), so host launch overhead cannot starve the GPU.
+    per_graph = 1 if args.no_graph else min(PER_GRAPH, args.steps)
+    graph_step = graph_attend = graph_rem = None
+    rem = args.steps % per_graph
     if not args.no_graph:
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
@@ -306,15 +310,23 @@ def main():
         torch.cuda.synchronize()
         graph_step, graph_attend = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph_step):
-            step()
+            for _ in range(per_graph):
+                step()
         with torch.cuda.graph(graph_attend):
-            attend_only()
+            for _ in range(per_graph):
+                attend_only()
+        if rem:
+            graph_rem = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_rem):
+                for _ in range(rem):
+                    step()
         torch.cuda.synchronize()
-        for _ in range(args.warmup):
+        for _ in range(max(1, args.warmup // per_graph)):
             graph_step.replay()
         torch.cuda.synchronize()
-    run_step = graph_step.replay if graph_step is not None else step
-    run_attend = graph_attend.replay if graph_attend is not None else attend_only
+    run_steps = graph_step.replay if graph_step is not None else step
+    run_rem = graph_rem.replay if graph_rem is not None else (lambda: None)
+    run_attends = graph_attend.replay if graph_attend is not None else attend_only
 
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -324,8 +336,9 @@ def main():
     clocks.start()
     time.sleep(0.3)  # let the sampler take its first reading
     t_start.record(stream)
-    for i in range(args.steps):
-        run_step()
+    for i in range(args.steps // per_graph):  # exactly args.steps steps
+        run_steps()
+    run_rem()
     t_end.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
@@ -338,14 +351,14 @@ def main():
 
     # Average duration of the dominant kernel (attention step), CUDA events on
     # the launching stream around back-to-back launches.
-    n_att = max(10, min(args.steps, 2000))
+    n_rep = max(1, min(args.steps, 2000) // per_graph)
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(stream)
-    for _ in range(n_att):
-        run_attend()
+    for _ in range(n_rep):
+        run_attends()
     a1.record(stream)
     torch.cuda.synchronize()
-    attend_s = a0.elapsed_time(a1) / 1e3 / n_att
+    attend_s = a0.elapsed_time(a1) / 1e3 / (n_rep * per_graph)
     if dist is not None:
         t = torch.tensor([elapsed], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -438,7 +451,7 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3},
         "gpu_launches": args.steps * (1 + binding.lib().mla_decode_kernels_per_run()),
-        "launch_mode": "cuda_graph" if graph_step is not None else "host",
+        "launch_mode": ("cuda_graph, %d steps per replay" % per_graph) if graph_step is not None else "host",
         "clocks": clocks.summary(),
     }
     if breakdown is not None:

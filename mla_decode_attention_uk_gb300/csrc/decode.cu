@@ -52,6 +52,14 @@ constexpr int kMaxSlots = 4;
 constexpr int kSBufs = 2;                          // S buffers, each two 64-column K halves
 constexpr int kPTBytes = 64 * 128;                 // one P^T buffer: 64 rows x 64 keys bf16
 constexpr int kMaxPT = 2;
+constexpr int kFreeGroups = 5;                     // slot release groups (see slot_free)
+// Box orders as nibble lists (first box in the lowest nibble).  The producer
+// loads boxes in release order: RoPE box, PV blocks 0 and 2, then 1 and 3.
+// Each QK^T issuer takes its boxes (0-4 / 5-8) in the same order.
+constexpr uint64_t kLoadOrder = 0x763254108ull;    // 8, 0, 1, 4, 5, 2, 3, 6, 7
+constexpr uint64_t kQkOrder0 = 0x32410ull;         // 0, 1, 4, 2, 3
+constexpr uint64_t kQkOrder1 = 0x7658ull;          // 8, 5, 6, 7
+__host__ __device__ constexpr int free_group(int box) { return box == 8 ? 4 : box >> 1; }
 #ifndef MLA_PREFETCH_PAGES
 #define MLA_PREFETCH_PAGES 2
 #endif
@@ -130,9 +138,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
               DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
-  // slot_full has one barrier per box, so QK^T can start on the first boxes of
-  // a page while the rest are still in flight.
-  __shared__ __align__(8) uint64_t q_full, q_free, slot_full[kMaxSlots][kBoxes], slot_empty[kMaxSlots],
+  // Page slots are filled and released box by box: slot_full has one barrier
+  // per box, so QK^T starts on the first boxes of a page while the rest are in
+  // flight; slot_free has one per release group (latent boxes 2m, 2m+1 after
+  // PV block m; the RoPE box after QK^T), so the next page's boxes start
+  // loading as soon as their group is free.
+  __shared__ __align__(8) uint64_t q_full, q_free, slot_full[kMaxSlots][kBoxes],
+      slot_free[kMaxSlots][kFreeGroups],
       s_full[kSBufs], s_free[kSBufs], p_full[kMaxPT], p_free[kMaxPT], o_full, o_free,
       drain_bar[4];
   __shared__ uint32_t tmem_base_sh;
@@ -168,7 +180,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     mbar_init(smem_u32(&q_free), 2);
     for (int i = 0; i < NS; ++i) {
       for (int j = 0; j < kBoxes; ++j) mbar_init(smem_u32(&slot_full[i][j]), 1);
-      mbar_init(smem_u32(&slot_empty[i]), 2);
+      for (int r = 0; r < kFreeGroups; ++r) mbar_init(smem_u32(&slot_free[i][r]), 1);
     }
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(smem_u32(&s_full[i]), 2);
@@ -240,20 +252,31 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           }
           for (int i = 0; i < cr.nchunks; ++i, ++g) {
             const int s = g % NS, u = g / NS;
-            if (u > 0 && !mbar_wait(smem_u32(&slot_empty[s]), (u - 1) & 1, &abort_sh, P.status)) {
-              ok = false;
-              break;
-            }
             const int row = ahead[0] * kPage;
             const uint32_t dst = sSlot0 + s * kSlotBytes;
-            // Boxes in the order the two QK^T issuers consume them (0-4 and
-            // 5-8 interleaved).
-#pragma unroll 1
-            for (int t = 0; t < kBoxes; ++t) {
-              const int j = (t & 1) ? 5 + (t >> 1) : (t >> 1);
+            // Each box is loaded as soon as its release group of the slot's
+            // previous page is free.
+            int t = 0;
+            for (int prev = -1; t < kBoxes; ++t) {
+              const int j = static_cast<int>((kLoadOrder >> (4 * t)) & 15);
+              const int grp = free_group(j);
+              if (u > 0 && grp != prev) {
+                if (!mbar_wait(smem_u32(&slot_free[s][grp]), (u - 1) & 1, &abort_sh, P.status)) {
+                  ok = false;
+                  break;
+                }
+                prev = grp;
+              }
               const uint32_t fb = smem_u32(&slot_full[s][j]);
               mbar_expect_tx(fb, kChunkBox);
               tma_load_2d(dst + j * kChunkBox, &tm_c, j * kBoxCols, row, fb);
+            }
+            if (!ok) {
+              // Boxes of this page already in flight land before the CTA exits.
+              for (int t2 = 0; t2 < t; ++t2)
+                mbar_wait_drain(smem_u32(&slot_full[s][(kLoadOrder >> (4 * t2)) & 15]), u & 1,
+                                P.status);
+              break;
             }
             // Shift the look-ahead window and fetch (and L2-prefetch) the page
             // kLookAhead chunks ahead.
@@ -300,7 +323,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const uint32_t qbox16 = q_box_bytes >> 4;
       const bool is_qk = warp == 1 || warp == 2;
       const int half = (warp == 1 || warp == 3) ? 0 : 1;  // K half (QK) / latent half (PV)
-      const int j0 = half == 0 ? 0 : 5, j1 = half == 0 ? 5 : kBoxes;  // QK boxes
+      const uint64_t qk_order = half == 0 ? kQkOrder0 : kQkOrder1;  // QK boxes
+      const int qk_boxes = half == 0 ? 5 : 4;
       int g = 0, pc = 0;
       bool ok = true;
       for (int k = k0; k < R && ok; k += G) {
@@ -320,8 +344,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               }
               const uint64_t bd0 = dslot0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
               const uint32_t d = tmem + 128 * sb + 64 * half;
-              for (int j = j0; j < j1 && ok; ++j) {
+              for (int t = 0; t < qk_boxes && ok; ++t) {
                 // Each box's MMAs go out as soon as that box has landed.
+                const int j = static_cast<int>((qk_order >> (4 * t)) & 15);
                 if (!mbar_wait(smem_u32(&slot_full[s][j]), (g / NS) & 1, &abort_sh, P.status)) {
                   ok = false;
                   break;
@@ -330,10 +355,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                   umma_bf16(d, dq0 + (j * qbox16 + kk * 2), bd0 + ((j * kChunkBox) >> 4) + kk * 2,
-                            idesc_qk, (j != j0) || (kk != 0));
+                            idesc_qk, (t != 0) || (kk != 0));
                 }
               }
               if (!ok) break;
+              // The RoPE box is read by this issuer's QK^T only.
+              if (half == 1) umma_commit(smem_u32(&slot_free[s][free_group(8)]));
               umma_commit(smem_u32(&s_full[sb]));
             }
             if (!ok) break;
@@ -361,9 +388,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                   umma_bf16(tmem + kTmemO + 64 * m, ad0 + ((2 * m * kChunkBox + kk * 2048) >> 4),
                             bd0 + kk * 2, idesc_pv, !(first && kk == 0));
                 }
+                umma_commit(smem_u32(&slot_free[s][m]));  // latent boxes 2m, 2m+1
               }
               umma_commit(smem_u32(&p_free[pb2]));
-              umma_commit(smem_u32(&slot_empty[s]));
             }
             if (!ok) break;
             umma_commit(smem_u32(&o_full));
