@@ -26,8 +26,9 @@
 //     when the max grows by more than 2^8), P written to shared memory as bf16.
 //   * PV on tcgen05, transposed: O^T[latent, row] += C^T[latent, key] P^T[key, row]
 //     with the page slot read MN-major as the A operand (M = 128 latent, four
-//     MMAs for 512) and N = 64 rows; O^T lives in 256 TMEM columns.  P^T is
-//     double-buffered when the query tile is small enough to leave room.
+//     MMAs for 512) and N = 64 rows; O^T lives in 256 TMEM columns.  P^T of a
+//     page is written into that page's RoPE box (dead once QK^T is done), so
+//     every page in flight has its own P^T buffer at no extra shared memory.
 //   * Epilogue (warps 4-7): O / l to bf16 o_lat plus lse for unsplit sequences,
 //     or fp32 partials for split ones.
 // Warp roles: 0 TMA producer, 1-2 QK^T issuers (K halves; warp 2 also owns
@@ -50,16 +51,16 @@ constexpr int kChunkBox = kChunk * 128;            // one 64 x 64 bf16 box: 8 KB
 constexpr int kSlotBytes = kBoxes * kChunkBox;     // 72 KB
 constexpr int kMaxSlots = 4;
 constexpr int kSBufs = 2;                          // S buffers, each two 64-column K halves
-constexpr int kPTBytes = 64 * 128;                 // one P^T buffer: 64 rows x 64 keys bf16
-constexpr int kMaxPT = 2;
+constexpr int kRopeBox = kBoxes - 1;               // box 8: the 64 RoPE columns, then P^T
 constexpr int kFreeGroups = 5;                     // slot release groups (see slot_free)
 // Box orders as nibble lists (first box in the lowest nibble).  The producer
-// loads boxes in release order: RoPE box, PV blocks 0 and 2, then 1 and 3.
-// Each QK^T issuer takes its boxes (0-4 / 5-8) in the same order.
-constexpr uint64_t kLoadOrder = 0x763254108ull;    // 8, 0, 1, 4, 5, 2, 3, 6, 7
+// loads boxes in release order: PV blocks 0 and 2, then 1 and 3, then the
+// RoPE box (it holds the page's P^T until PV is done).  Each QK^T issuer
+// takes its boxes (0-4 / 5-8) in the same order.
+constexpr uint64_t kLoadOrder = 0x876325410ull;    // 0, 1, 4, 5, 2, 3, 6, 7, 8
 constexpr uint64_t kQkOrder0 = 0x32410ull;         // 0, 1, 4, 2, 3
-constexpr uint64_t kQkOrder1 = 0x7658ull;          // 8, 5, 6, 7
-__host__ __device__ constexpr int free_group(int box) { return box == 8 ? 4 : box >> 1; }
+constexpr uint64_t kQkOrder1 = 0x8765ull;          // 5, 6, 7, 8
+__host__ __device__ constexpr int free_group(int box) { return box == kRopeBox ? 4 : box >> 1; }
 #ifndef MLA_PREFETCH_PAGES
 #define MLA_PREFETCH_PAGES 2
 #endif
@@ -86,7 +87,7 @@ struct DecodeParams {
   float* opart;              // [slots, T*H, 512]
   float* lpart;              // [slots, T*H]
   int32_t* status;
-  int B, T, H, max_pages, num_pages, tiles, q_box_rows, num_slots, num_pt;
+  int B, T, H, max_pages, num_pages, tiles, q_box_rows, num_slots;
   float scale, scale_log2;
 };
 
@@ -141,11 +142,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   // Page slots are filled and released box by box: slot_full has one barrier
   // per box, so QK^T starts on the first boxes of a page while the rest are in
   // flight; slot_free has one per release group (latent boxes 2m, 2m+1 after
-  // PV block m; the RoPE box after QK^T), so the next page's boxes start
-  // loading as soon as their group is free.
+  // PV block m; the RoPE box, which holds the page's P^T once QK^T is done,
+  // after both PV issuers), so the next page's boxes start loading as soon as
+  // their group is free.  p_full / p_free (P^T written / PV done) follow the
+  // slot of the page.
   __shared__ __align__(8) uint64_t q_full, q_free, slot_full[kMaxSlots][kBoxes],
       slot_free[kMaxSlots][kFreeGroups],
-      s_full[kSBufs], s_free[kSBufs], p_full[kMaxPT], p_free[kMaxPT], o_full, o_free,
+      s_full[kSBufs], s_free[kSBufs], p_full[kMaxSlots], p_free[kMaxSlots], o_full, o_free,
       drain_bar[4];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -161,7 +164,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int R = P.header->num_ranges;
   const int TH = P.T * P.H;
   const int NS = P.num_slots;
-  const int NPT = P.num_pt;                       // P^T buffers (1 or 2)
   {
     const WsLayout L = make_layout(P.B, P.T, P.H, R);
     P.range_b = reinterpret_cast<const int32_t*>(P.ws + L.range_b);
@@ -173,20 +175,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = sbase;
   const uint32_t sSlot0 = sQ + kBoxes * q_box_bytes;
-  const uint32_t sPT = sSlot0 + NS * kSlotBytes;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&q_full), 1);
     mbar_init(smem_u32(&q_free), 2);
     for (int i = 0; i < NS; ++i) {
       for (int j = 0; j < kBoxes; ++j) mbar_init(smem_u32(&slot_full[i][j]), 1);
-      for (int r = 0; r < kFreeGroups; ++r) mbar_init(smem_u32(&slot_free[i][r]), 1);
+      for (int r = 0; r < kFreeGroups; ++r)
+        mbar_init(smem_u32(&slot_free[i][r]), r == free_group(kRopeBox) ? 2 : 1);
     }
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(smem_u32(&s_full[i]), 2);
       mbar_init(smem_u32(&s_free[i]), 4);
     }
-    for (int i = 0; i < NPT; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&p_full[i]), 1);
       mbar_init(smem_u32(&p_free[i]), 2);
     }
@@ -319,7 +321,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dslot0 = sdesc_sw128(sSlot0, 16, 1024);
       const uint64_t dpv0 = sdesc_sw128(sSlot0, kChunkBox, 1024);
-      const uint64_t dpt0 = sdesc_sw128(sPT, 16, 1024);
       const uint32_t qbox16 = q_box_bytes >> 4;
       const bool is_qk = warp == 1 || warp == 2;
       const int half = (warp == 1 || warp == 3) ? 0 : 1;  // K half (QK) / latent half (PV)
@@ -359,8 +360,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
               }
               if (!ok) break;
-              // The RoPE box is read by this issuer's QK^T only.
-              if (half == 1) umma_commit(smem_u32(&slot_free[s][free_group(8)]));
               umma_commit(smem_u32(&s_full[sb]));
             }
             if (!ok) break;
@@ -369,18 +368,19 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             umma_commit(smem_u32(&q_free));
           } else {
             for (int i = 0; i < nc; ++i, ++g) {
-              const int pb2 = g % NPT;  // P^T buffer used by this chunk
+              const int s = g % NS;
               const bool first = i == 0;
-              if (!mbar_wait(smem_u32(&p_full[pb2]), (g / NPT) & 1, &abort_sh, P.status) ||
+              if (!mbar_wait(smem_u32(&p_full[s]), (g / NS) & 1, &abort_sh, P.status) ||
                   (first && pc > 0 &&
                    !mbar_wait(smem_u32(&o_free), (pc - 1) & 1, &abort_sh, P.status))) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              const int s = g % NS;
               const uint64_t ad0 = dpv0 + static_cast<uint64_t>((s * kSlotBytes) >> 4);
-              const uint64_t bd0 = dpt0 + static_cast<uint64_t>((pb2 * kPTBytes) >> 4);
+              // P^T of this page sits in its slot's RoPE box.
+              const uint64_t bd0 =
+                  dslot0 + static_cast<uint64_t>((s * kSlotBytes + kRopeBox * kChunkBox) >> 4);
 #pragma unroll
               for (int m = 2 * half; m < 2 * half + 2; ++m) {
 #pragma unroll
@@ -390,7 +390,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
                 umma_commit(smem_u32(&slot_free[s][m]));  // latent boxes 2m, 2m+1
               }
-              umma_commit(smem_u32(&p_free[pb2]));
+              umma_commit(smem_u32(&slot_free[s][free_group(kRopeBox)]));  // P^T read
+              umma_commit(smem_u32(&p_free[s]));
             }
             if (!ok) break;
             umma_commit(smem_u32(&o_full));
@@ -497,13 +498,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               const float recv = __shfl_xor_sync(0xffffffffu, send, 2);
               packed[q] = par ? pack_bf16x2(recv, p[16 + q]) : pack_bf16x2(p[q], recv);
             }
-            // P^T buffer pb2 is free once the PV that last read it has finished.
-            const int pb2 = g % NPT;
-            if (g >= NPT && !mbar_wait(smem_u32(&p_free[pb2]), ((g / NPT) - 1) & 1, &abort_sh,
-                                       P.status))
-              bad = true;
+            // P^T goes into the page's RoPE box: QK^T, its only reader, is
+            // complete (S is), and the box is not refilled before PV is done.
             if (!bad) {
-              const uint32_t rowaddr = sPT + pb2 * kPTBytes + srow_c * 128;
+              const uint32_t rowaddr =
+                  sSlot0 + (g % NS) * kSlotBytes + kRopeBox * kChunkBox + srow_c * 128;
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 const int lchunk = 4 * par + q;
@@ -519,7 +518,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // quarters) once the previous chunk's PV has landed.
             bool f = *static_cast<volatile int*>(&abort_sh) != 0;
             if (!f && g >= 1 &&
-                !mbar_wait(smem_u32(&p_free[(g - 1) % NPT]), ((g - 1) / NPT) & 1, &abort_sh,
+                !mbar_wait(smem_u32(&p_free[(g - 1) % NS]), ((g - 1) / NS) & 1, &abort_sh,
                            P.status))
               f = true;
             if (bar_any(1, 128, f)) { fail = true; break; }
@@ -544,7 +543,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           }
           // The barrier above ordered all four warps' P^T writes (and any
           // rescale) before this point: one arrival releases the PV issuers.
-          if (threadIdx.x == 128) mbar_arrive(smem_u32(&p_full[g % NPT]));
+          if (threadIdx.x == 128) mbar_arrive(smem_u32(&p_full[g % NS]));
         }
         if (fail) break;
 
@@ -623,20 +622,14 @@ int decode_q_box_rows(int T, int H) {
   const int r = T * H;
   return r >= kTileRows ? kTileRows : ((r + 7) / 8) * 8;
 }
-// Page slots and P^T buffers that fit next to the query tile: two P^T
-// buffers when two page slots still fit, else one.
-int decode_num_pt(int T, int H) {
-  const int q_bytes = kBoxes * decode_q_box_rows(T, H) * 128;
-  return (kDynSmemMax - 1024 - q_bytes - 2 * kPTBytes) / kSlotBytes >= 2 ? 2 : 1;
-}
+// Page slots that fit next to the query tile.
 int decode_num_slots(int T, int H) {
   const int q_bytes = kBoxes * decode_q_box_rows(T, H) * 128;
-  int ns = (kDynSmemMax - 1024 - q_bytes - decode_num_pt(T, H) * kPTBytes) / kSlotBytes;
+  int ns = (kDynSmemMax - 1024 - q_bytes) / kSlotBytes;
   return ns > kMaxSlots ? kMaxSlots : ns;
 }
 int decode_smem_bytes(int T, int H) {
-  return 1024 + kBoxes * decode_q_box_rows(T, H) * 128 + decode_num_slots(T, H) * kSlotBytes +
-         decode_num_pt(T, H) * kPTBytes;
+  return 1024 + kBoxes * decode_q_box_rows(T, H) * 128 + decode_num_slots(T, H) * kSlotBytes;
 }
 // Largest number of co-resident CTA groups (one CTA per tile of a sequence's
 // query rows; one CTA per SM).
@@ -684,7 +677,6 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
   P.tiles = decode_tiles(T, H);
   P.q_box_rows = decode_q_box_rows(T, H);
   P.num_slots = decode_num_slots(T, H);
-  P.num_pt = decode_num_pt(T, H);
   P.scale = scale;
   P.scale_log2 = scale * 1.4426950408889634f;
 
