@@ -225,8 +225,6 @@ int mla_decode_plan_ex(const mla_decode_dims* d, const int32_t* seq_lens, int32_
   const WsLayout L = make_layout(d->batch, d->q_len, d->num_heads, R);
   if (ws_bytes < L.total) return MLA_DECODE_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(at<int32_t>(ws, L.status), 0, sizeof(int32_t), st) != cudaSuccess)
-    return cuda_rc(cudaErrorUnknown);
   return cuda_rc(launch_plan(seq_lens, d->batch, d->q_len, d->max_pages_per_seq, R,
                              at<int32_t>(ws, L.status), at<PlanHeader>(ws, L.header),
                              at<int32_t>(ws, L.range_b), at<int32_t>(ws, L.range_p),

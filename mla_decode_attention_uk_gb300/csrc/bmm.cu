@@ -54,7 +54,11 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
-  griddep_wait();
+  // The up-projection reads o_lat from the step before it.  The absorb step
+  // reads only the caller's q and W_UK, so it starts at once and overlaps the
+  // planner; it waits for its predecessor just before exiting, so that its
+  // completion still implies the planner's (the attention step relies on it).
+  if constexpr (MODE == BmmMode::kUpProject) griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tok0 = blockIdx.x * NT;
@@ -185,6 +189,7 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if constexpr (MODE == BmmMode::kAbsorb) griddep_wait();
 }
 
 template <BmmMode MODE, int NT>

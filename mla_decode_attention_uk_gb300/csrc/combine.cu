@@ -69,30 +69,47 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
   const float* __restrict__ opart = reinterpret_cast<const float*>(ws + L.opart);
   const float* __restrict__ lpart = reinterpret_cast<const float*>(ws + L.lpart);
 
+  // Lane s holds the lse of split s (32 splits per pass), so the loads go out
+  // together and the max and sum are warp reductions.
   float m = -INFINITY;
-  for (int s = 0; s < ns; ++s) m = fmaxf(m, lpart[static_cast<size_t>(slot0 + s) * TH + r]);
+  for (int s0 = 0; s0 < ns; s0 += 32) {
+    const float l = s0 + lane < ns ? lpart[static_cast<size_t>(slot0 + s0 + lane) * TH + r]
+                                   : -INFINITY;
+    m = fmaxf(m, l);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float wsum = 0.0f;
-  for (int s = 0; s < ns; ++s) {
-    const float l = lpart[static_cast<size_t>(slot0 + s) * TH + r];
+  for (int s0 = 0; s0 < ns; s0 += 32) {
+    const float l = s0 + lane < ns ? lpart[static_cast<size_t>(slot0 + s0 + lane) * TH + r]
+                                   : -INFINITY;
     wsum += (l == -INFINITY) ? 0.0f : __expf(l - m);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
   const float lse = m + __logf(wsum);
 
   float4 acc[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < ns; ++s) {
-    const float l = lpart[static_cast<size_t>(slot0 + s) * TH + r];
-    const float w = (l == -INFINITY) ? 0.0f : __expf(l - lse);
-    const float4* src =
-        reinterpret_cast<const float4*>(opart + (static_cast<size_t>(slot0 + s) * TH + r) * kLora);
+  for (int s0 = 0; s0 < ns; s0 += 32) {
+    const float l = s0 + lane < ns ? lpart[static_cast<size_t>(slot0 + s0 + lane) * TH + r]
+                                   : -INFINITY;
+    const float wl = (l == -INFINITY) ? 0.0f : __expf(l - lse);  // weight of split s0 + lane
+    const int n = min(32, ns - s0);
+#pragma unroll 4
+    for (int i = 0; i < n; ++i) {
+      const float w = __shfl_sync(0xffffffffu, wl, i);
+      const float4* src = reinterpret_cast<const float4*>(
+          opart + (static_cast<size_t>(slot0 + s0 + i) * TH + r) * kLora);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 v = src[q * 32 + lane];
-      acc[q].x += w * v.x;
-      acc[q].y += w * v.y;
-      acc[q].z += w * v.z;
-      acc[q].w += w * v.w;
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = src[q * 32 + lane];
+        acc[q].x += w * v.x;
+        acc[q].y += w * v.y;
+        acc[q].z += w * v.z;
+        acc[q].w += w * v.w;
+      }
     }
   }
 

@@ -19,6 +19,9 @@ namespace mla {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+// Batches up to this size keep the cost prefix and page counts in shared
+// memory, so the per-range binary searches do not chain global loads.
+constexpr int kPlanSmemB = 4096;
 
 // Inclusive block-wide scan of one int per thread (1024 threads).
 __device__ int block_inclusive_scan(int v, int* warp_tot) {
@@ -54,10 +57,19 @@ plan_kernel(const int32_t* __restrict__ seq_lens, int B, int T, int max_pages, i
             int32_t* __restrict__ prefix /* [B+1] */) {
   __shared__ int warp_tot[32];
   __shared__ int carry;
+  __shared__ int s_prefix[kPlanSmemB + 1];
+  __shared__ int s_pages[kPlanSmemB];
+  // Clear the status word once the previous step is done with it, then let
+  // the absorb step start: it does not read the plan and overlaps this kernel.
   griddep_wait();
-  griddep_launch_dependents();
-  if (threadIdx.x == 0) carry = 0;
+  if (threadIdx.x == 0) {
+    *status = MLA_STATUS_OK;
+    carry = 0;
+  }
   __syncthreads();
+  griddep_launch_dependents();
+  const bool in_smem = B <= kPlanSmemB;
+  int* pref = in_smem ? s_prefix : prefix;
 
   // Pass 1: sanitised lengths and the exclusive prefix of per-sequence cost.
   for (int base = 0; base < B; base += kPlanThreads) {
@@ -71,16 +83,18 @@ plan_kernel(const int32_t* __restrict__ seq_lens, int B, int T, int max_pages, i
         L = L < T ? T : cap;
       }
       seq_len_eff[b] = L;
-      cost = (L + kPage - 1) / kPage + kPieceCost;
+      const int pages = (L + kPage - 1) / kPage;
+      if (in_smem) s_pages[b] = pages;
+      cost = pages + kPieceCost;
     }
     const int incl = block_inclusive_scan(cost, warp_tot);
-    if (b < B) prefix[b] = carry + incl - cost;
+    if (b < B) pref[b] = carry + incl - cost;
     __syncthreads();
     if (threadIdx.x == kPlanThreads - 1) carry += incl;
     __syncthreads();
   }
   const int total = carry;
-  if (threadIdx.x == 0) prefix[B] = total;
+  if (threadIdx.x == 0) pref[B] = total;
   const int per = (total + R - 1) / R > 0 ? (total + R - 1) / R : 1;
   __syncthreads();
 
@@ -92,11 +106,11 @@ plan_kernel(const int32_t* __restrict__ seq_lens, int B, int T, int max_pages, i
       int lo = 0, hi = B - 1;  // largest b with prefix[b] <= x
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (prefix[mid] <= x) lo = mid; else hi = mid - 1;
+        if (pref[mid] <= x) lo = mid; else hi = mid - 1;
       }
       b = lo;
-      p = static_cast<int>(x - prefix[b]);
-      const int pages = (seq_len_eff[b] + kPage - 1) / kPage;
+      p = static_cast<int>(x - pref[b]);
+      const int pages = in_smem ? s_pages[b] : (seq_len_eff[b] + kPage - 1) / kPage;
       if (p >= pages) { b += 1; p = 0; }
     }
     range_b[k] = b;
@@ -110,9 +124,9 @@ plan_kernel(const int32_t* __restrict__ seq_lens, int B, int T, int max_pages, i
     const int b = base + threadIdx.x;
     int ns = 0;
     if (b < B) {
-      const int pages = (seq_len_eff[b] + kPage - 1) / kPage;
-      const int kf = prefix[b] / per;
-      const int kl = (prefix[b] + pages - 1) / per;
+      const int pages = in_smem ? s_pages[b] : (seq_len_eff[b] + kPage - 1) / kPage;
+      const int kf = pref[b] / per;
+      const int kl = (pref[b] + pages - 1) / per;
       ns = kl - kf + 1;
       seq_first[b] = kf;
       seq_nsplit[b] = ns;
