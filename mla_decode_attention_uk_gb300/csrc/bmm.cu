@@ -54,11 +54,11 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
-  // The up-projection reads o_lat from the step before it.  The absorb step
-  // reads only the caller's q and W_UK, so it starts at once and overlaps the
-  // planner; it waits for its predecessor just before exiting, so that its
-  // completion still implies the planner's (the attention step relies on it).
-  if constexpr (MODE == BmmMode::kUpProject) griddep_wait();
+  // Neither step waits for its predecessor up front.  The absorb step reads
+  // only the caller's q and W_UK, so it overlaps the planner; it waits for
+  // its predecessor just before exiting, so that its completion still implies
+  // the planner's (the attention step relies on it).  The up-projection loads
+  // its first weight tiles, then waits (producer thread) before loading o_lat.
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tok0 = blockIdx.x * NT;
@@ -93,7 +93,23 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
 
   if (warp == 0) {
     if (elect_one()) {
-      for (int kc = 0; kc < nk; ++kc) {
+      int kc0 = 0;
+      if constexpr (MODE == BmmMode::kUpProject) {
+        kc0 = nk < STAGES ? nk : STAGES;
+        for (int kc = 0; kc < kc0; ++kc) {
+          const uint32_t a = sbase + kc * S::kStageBytes;
+          const uint32_t fb = smem_u32(&full_bar[kc]);
+          mbar_expect_tx(fb, S::kStageBytes);
+          tma_load_2d(a, &tm_w, m0, h * K + kc * 64, fb);
+          tma_load_2d(a + kBoxBytes, &tm_w, m0 + 64, h * K + kc * 64, fb);
+        }
+        griddep_wait();  // o_lat comes from the step before
+        for (int kc = 0; kc < kc0; ++kc) {
+          const uint32_t b = sbase + kc * S::kStageBytes + kABytes;
+          tma_load_2d(b, &tm_x, h * Kx + kc * 64, tok0, smem_u32(&full_bar[kc]));
+        }
+      }
+      for (int kc = kc0; kc < nk; ++kc) {
         const int s = kc % STAGES;
         if (kc >= STAGES &&
             !mbar_wait(smem_u32(&empty_bar[s]), ((kc / STAGES) - 1) & 1, &abort_sh, status))

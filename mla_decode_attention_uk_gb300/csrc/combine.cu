@@ -33,23 +33,30 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
                const uint8_t* __restrict__ ws, const PlanHeader* __restrict__ header, int B,
                int T, int H, const __nv_bfloat16* __restrict__ qlo,
                __nv_bfloat16* __restrict__ olat, float* __restrict__ lse_out, float scale) {
-  griddep_wait();
+  // The plan and q_lo are complete when this kernel starts (the attention
+  // step waited for them before letting it launch), so they are read before
+  // waiting for the attention step itself.
   griddep_launch_dependents();
   const int TH = T * H;
   const int b = blockIdx.y;
   const int r = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (r >= TH) return;
+  if (r >= TH) {
+    griddep_wait();
+    return;
+  }
   const int ns = seq_nsplit[b];
   const size_t row = static_cast<size_t>(b) * TH + r;
   if (ns <= 1) {
     // Unsplit: o_lat and lse were written by the attention step.
     const uint4* o4 = reinterpret_cast<const uint4*>(olat + row * kLora) + lane * 2;
     const uint4* l4 = reinterpret_cast<const uint4*>(qlo + row * kLora) + lane * 2;
+    const uint4 lv0 = l4[0], lv1 = l4[1];
+    griddep_wait();
     float corr = 0.0f;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const uint4 ov = o4[q], lv = l4[q];
+      const uint4 ov = o4[q], lv = q == 0 ? lv0 : lv1;
       const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
       const uint32_t lw[4] = {lv.x, lv.y, lv.z, lv.w};
 #pragma unroll
@@ -65,6 +72,11 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
     return;
   }
   const int slot0 = seq_slot[b];
+  uint2 lo_raw[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    lo_raw[q] = *reinterpret_cast<const uint2*>(qlo + row * kLora + (q * 32 + lane) * 4);
+  griddep_wait();
   const WsLayout L = make_layout(B, T, H, header->num_ranges);
   const float* __restrict__ opart = reinterpret_cast<const float*>(ws + L.opart);
   const float* __restrict__ lpart = reinterpret_cast<const float*>(ws + L.lpart);
@@ -117,9 +129,8 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int col = (q * 32 + lane) * 4;
-    const uint2 lo_raw = *reinterpret_cast<const uint2*>(qlo + row * kLora + col);
-    const __nv_bfloat162 l01 = *reinterpret_cast<const __nv_bfloat162*>(&lo_raw.x);
-    const __nv_bfloat162 l23 = *reinterpret_cast<const __nv_bfloat162*>(&lo_raw.y);
+    const __nv_bfloat162 l01 = *reinterpret_cast<const __nv_bfloat162*>(&lo_raw[q].x);
+    const __nv_bfloat162 l23 = *reinterpret_cast<const __nv_bfloat162*>(&lo_raw[q].y);
     corr += __low2float(l01) * acc[q].x + __high2float(l01) * acc[q].y +
             __low2float(l23) * acc[q].z + __high2float(l23) * acc[q].w;
     __nv_bfloat162 o01 = __floats2bfloat162_rn(acc[q].x, acc[q].y);

@@ -155,22 +155,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   __shared__ float alpha_sh[64];
   __shared__ float inv_l_sh[64];
 
-  griddep_wait();
-  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x % P.tiles;
   const int k0 = blockIdx.x / P.tiles;
   const int G = gridDim.x / P.tiles;
-  const int R = P.header->num_ranges;
   const int TH = P.T * P.H;
   const int NS = P.num_slots;
-  {
-    const WsLayout L = make_layout(P.B, P.T, P.H, R);
-    P.range_b = reinterpret_cast<const int32_t*>(P.ws + L.range_b);
-    P.range_p = reinterpret_cast<const int32_t*>(P.ws + L.range_p);
-    P.lpart = reinterpret_cast<float*>(P.ws + L.lpart);
-    P.opart = reinterpret_cast<float*>(P.ws + L.opart);
-  }
   const uint32_t q_box_bytes = static_cast<uint32_t>(P.q_box_rows) * 128u;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = sbase;
@@ -199,6 +189,19 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_c);
+  }
+  // Everything above overlaps the previous step's tail.  The plan, q_lat and
+  // (on this SM) the tensor memory of the absorb step are only safe to use
+  // once it has completed.
+  griddep_wait();
+  griddep_launch_dependents();
+  const int R = P.header->num_ranges;
+  {
+    const WsLayout L = make_layout(P.B, P.T, P.H, R);
+    P.range_b = reinterpret_cast<const int32_t*>(P.ws + L.range_b);
+    P.range_p = reinterpret_cast<const int32_t*>(P.ws + L.range_p);
+    P.lpart = reinterpret_cast<float*>(P.ws + L.lpart);
+    P.opart = reinterpret_cast<float*>(P.ws + L.opart);
   }
   if (warp == 2) {
     tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
