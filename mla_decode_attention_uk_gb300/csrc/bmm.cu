@@ -212,7 +212,9 @@ template <BmmMode MODE, int NT>
 cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, int H, int K,
                           int Kx, int Mtot, const __nv_bfloat16* q, __nv_bfloat16* hi,
                           __nv_bfloat16* lo, int32_t* status, cudaStream_t st) {
-  constexpr int STAGES = MODE == BmmMode::kAbsorb ? 2 : 4;
+  // Two stages for the absorb step (K = 128) and for 128-token tiles (64 KB of
+  // stages, three CTAs per SM); four for the up-projection's smaller tiles.
+  constexpr int STAGES = (MODE == BmmMode::kAbsorb || NT == 128) ? 2 : 4;
   auto kern = bmm_kernel<MODE, NT, STAGES>;
   const int smem = BmmSmem<NT, STAGES>::kTotal;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
