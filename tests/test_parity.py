@@ -80,6 +80,46 @@ def test_deterministic_for_a_fixed_plan():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+def test_one_plan_serves_consecutive_runs_bitwise():
+    # The plan is built once per decode step and reused by every layer: runs
+    # back to back on one plan (the absorb step of a run overlapping the end of
+    # the previous run) must give identical results.
+    inp = make_inputs(4, [100, 3000, 64, 777], 1, 128, seed=15)
+    dev = torch.device("cuda")
+    g = inp.to(dev)
+    d = binding.dims_for(g.q, g.cache, g.block_table)
+    m = binding.MlaDecode(d, dev)
+    outs = [torch.empty(4, 1, 128, 128, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    lses = [torch.empty(4, 1, 128, dtype=torch.float32, device=dev) for _ in range(3)]
+    m.plan(g.seq_lens)
+    for o, l in zip(outs, lses):
+        m.run(g.q, g.cache, g.block_table, g.seq_lens, g.w_uk, g.w_uv, g.scale, o, l)
+    assert m.check() == 0
+    for o, l in zip(outs[1:], lses[1:]):
+        assert torch.equal(o, outs[0]) and torch.equal(l, lses[0])
+    assert_parity(compare(inp, outs[0].cpu(), lses[0].cpu()), "plan reused")
+
+
+def test_step_calls_equal_run_bitwise():
+    inp = make_inputs(3, [500, 70, 1400], 2, 64, seed=16)
+    dev = torch.device("cuda")
+    g = inp.to(dev)
+    d = binding.dims_for(g.q, g.cache, g.block_table)
+    m = binding.MlaDecode(d, dev, 5)
+    o1 = torch.empty(3, 2, 64, 128, dtype=torch.bfloat16, device=dev)
+    l1 = torch.empty(3, 2, 64, dtype=torch.float32, device=dev)
+    o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
+    m.plan(g.seq_lens)
+    m.run(g.q, g.cache, g.block_table, g.seq_lens, g.w_uk, g.w_uv, g.scale, o1, l1)
+    m.plan(g.seq_lens)
+    m.absorb(g.q, g.w_uk)
+    m.attend(g.cache, g.block_table, g.seq_lens, g.scale, l2)
+    m.combine(g.scale, l2)
+    m.up_project(g.w_uv, o2)
+    assert m.check() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_page_permutation_same_schedule_bitwise():
     inp = make_inputs(3, [130, 640, 77], 1, 32, seed=10)
     o1, l1, _ = run_gpu(inp)
