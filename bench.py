@@ -217,6 +217,16 @@ def dist_setup(n_gpus):
     return 0, 1, 0, None
 
 
+def max_over_ranks(x, dist, dev):
+    """The largest value of x over all ranks (the job takes as long as its
+    slowest rank); x itself on a single process."""
+    if dist is None:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args):
     """The reference arm: the fp64 CPU oracle as it stands, on the host cores,
     each step a bounded row sample of the same workload."""
@@ -369,10 +379,7 @@ def main():
     a1.record(stream)
     torch.cuda.synchronize()
     attend_s = a0.elapsed_time(a1) / 1e3 / (n_rep * per_graph)
-    if dist is not None:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(elapsed, dist, dev)
     per_step = elapsed / args.steps
 
     # ---- end to end through the same C ABI with host buffers
@@ -404,10 +411,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_s = e0.elapsed_time(e1) / 1e3 / n_e2e
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, dist, dev)
 
     breakdown = None
     if args.breakdown:
