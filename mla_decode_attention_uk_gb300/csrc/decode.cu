@@ -11,8 +11,11 @@
 //
 // GB300 mapping (one CTA = 64 query rows of one sequence, one work range):
 //   * Keys stream page by page: the TMA producer gathers a 64-token page as 9
-//     boxes of 64 x 64 bf16 (128B swizzle) into a ring of 72 KB slots, looking
-//     the physical page up in the block table.  When the query rows of a
+//     boxes of 64 x 64 bf16 (128B swizzle) into a ring of 72 KB slots (two fit
+//     next to the query tile), looking the physical page up in the block
+//     table.  Slots fill and empty box by box: QK^T starts on a page's first
+//     boxes while the rest land, and the next page's boxes load as soon as
+//     their release group of the slot is free.  When the query rows of a
 //     sequence span 2 or 4 CTAs (tiles), those CTAs stream the same pages at
 //     about the same time and the second read of a page is served by L2; they
 //     are not coupled (a cluster sharing pages by multicast made every slot
@@ -32,8 +35,9 @@
 //   * Epilogue (warps 4-7): O / l to bf16 o_lat plus lse for unsplit sequences,
 //     or fp32 partials for split ones.
 // Warp roles: 0 TMA producer, 1-2 QK^T issuers (K halves; warp 2 also owns
-// TMEM), 3 and 8 PV issuers (latent halves), 4-7 softmax and epilogue.  The issuers work from precomputed descriptors so one
-// MMA costs an add and the issue itself.
+// TMEM), 3 and 8 PV issuers (latent halves), 4-7 softmax and epilogue.  The
+// issuers work from precomputed descriptors, so one MMA costs an add and the
+// issue itself.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
