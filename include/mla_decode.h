@@ -193,6 +193,15 @@ int mla_decode_run_static_scratch(const mla_decode_dims* dims, const void* q,
 /* Number of kernels one mla_decode_run enqueues (for launch accounting). */
 int mla_decode_kernels_per_run(void);
 
+/* Self-test of failure detection (no counterpart in the method): enqueues one
+ * small kernel that waits, through the library's bounded device-side wait, on
+ * a barrier that nothing ever completes.  The wait gives up after its limit
+ * (about 2 s), writes MLA_DECODE_TIMEOUT into *status (a device int32 that
+ * must hold 0 beforehand) and the kernel exits, leaving the context usable.
+ * Returns INVALID_ARG for a null or misaligned pointer, CUDA_ERROR if the
+ * launch fails, else OK (the status is written asynchronously). */
+int mla_decode_selftest_wait_timeout(int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,7 @@ ENTRY_POINTS = (
     "mla_decode_plan_ex", "mla_decode_run", "mla_decode_absorb", "mla_decode_attend",
     "mla_decode_combine", "mla_decode_up_project", "mla_decode_check", "mla_decode_status_string",
     "mla_decode_workspace_offsets", "mla_decode_kernels_per_run",
-    "mla_decode_run_static_scratch")
+    "mla_decode_run_static_scratch", "mla_decode_selftest_wait_timeout")
 
 
 class Dims(ctypes.Structure):
@@ -66,6 +66,7 @@ def lib():
         L.mla_decode_status_string.restype = ctypes.c_char_p
         L.mla_decode_workspace_offsets.argtypes = [D, i32, ctypes.POINTER(ctypes.c_int64), i32]
         L.mla_decode_run_static_scratch.argtypes = [D, P, P, P, P, P, P, ctypes.c_float, P, P, P]
+        L.mla_decode_selftest_wait_timeout.argtypes = [P, P]
         for n in ENTRY_POINTS:
             if n != "mla_decode_status_string":
                 getattr(L, n).restype = ctypes.c_int

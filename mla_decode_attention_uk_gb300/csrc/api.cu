@@ -10,6 +10,7 @@
 
 #include "../../include/mla_decode.h"
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace mla {
 cudaError_t launch_plan(const int32_t* seq_lens, int B, int T, int max_pages, int R,
@@ -37,6 +38,25 @@ cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, c
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
                            cudaStream_t st);
 }  // namespace mla
+
+namespace {
+
+// One thread waits, through the same bounded wait as every pipeline barrier
+// of the library, on an mbarrier that nothing ever arrives on.  The wait gives
+// up after its time limit, records TIMEOUT in *status and the kernel exits.
+__global__ void wait_timeout_kernel(int32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mla::mbar_init(mla::smem_u32(&bar), 1);
+    abort_flag = 0;
+    mla::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mla::mbar_wait(mla::smem_u32(&bar), 0, &abort_flag, status);
+}
+
+}  // namespace
 
 using namespace mla;
 
@@ -189,6 +209,12 @@ const char* mla_decode_status_string(int s) {
 }
 
 int mla_decode_kernels_per_run(void) { return 4; }
+
+int mla_decode_selftest_wait_timeout(int32_t* status, void* stream) {
+  if (!status || (reinterpret_cast<uintptr_t>(status) & 3u)) return MLA_DECODE_INVALID_ARG;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status);
+  return cuda_rc(cudaGetLastError());
+}
 
 int mla_decode_workspace_size_ex(const mla_decode_dims* d, int32_t num_ranges, size_t* bytes) {
   int rc = check_dims(d);

@@ -88,6 +88,8 @@ def test_null_pointers_rejected_before_any_launch():
                                 None) == 1
     assert L.mla_decode_up_project(ctypes.byref(d), fake, None, fake, 1 << 20, None) == 1
     assert L.mla_decode_check(None, None) == 1
+    assert L.mla_decode_selftest_wait_timeout(None, None) == 1
+    assert L.mla_decode_selftest_wait_timeout(ctypes.c_void_p(4098), None) == 1
 
 
 def test_misaligned_pointers_rejected():
