@@ -47,7 +47,10 @@ def test_tiny_workload_all_rows():
     assert_parity(compare(inp, out, lse), "tiny")
 
 
-@pytest.mark.parametrize("H,T", [(16, 1), (32, 1), (64, 1), (128, 1), (16, 2), (64, 2), (128, 2)])
+# 48/80 heads leave a partial last tile; 96 x 2 rows make three tiles; 112 x 2
+# rows make four with a 32-row last tile.
+@pytest.mark.parametrize("H,T", [(16, 1), (32, 1), (64, 1), (128, 1), (16, 2), (64, 2), (128, 2),
+                                 (48, 1), (80, 1), (96, 2), (112, 2)])
 def test_ragged_lengths_all_rows(H, T):
     lens = [T, 1 + T, 63, 64, 65, 127, 128, 129, 200, 511, 700]
     inp = make_inputs(len(lens), lens, T, H, seed=100 + H + T)
