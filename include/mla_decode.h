@@ -59,7 +59,8 @@ extern "C" {
 
 typedef struct {
   int32_t batch;             /* B >= 1: sequences in the decode batch            */
-  int32_t q_len;             /* T in {1, 2}: new query tokens per sequence        */
+  int32_t q_len;             /* T in 1..8: new query tokens per sequence; query t
+                                sees keys [0, seq_len - T + t] (causal block)     */
   int32_t num_heads;         /* H, multiple of 16, 16 <= H <= 128                 */
   int32_t qk_nope;           /* must be 128                                       */
   int32_t qk_rope;           /* must be 64                                        */

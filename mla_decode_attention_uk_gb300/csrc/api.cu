@@ -137,7 +137,7 @@ int check_dims(const mla_decode_dims* d) {
   if (d->qk_nope != kNope || d->qk_rope != kRope || d->kv_lora != kLora ||
       d->v_head != kVHead || d->page_size != kPage)
     return MLA_DECODE_UNSUPPORTED;
-  if (d->q_len < 1 || d->q_len > 2) return MLA_DECODE_UNSUPPORTED;
+  if (d->q_len < 1 || d->q_len > kMaxQLen) return MLA_DECODE_UNSUPPORTED;
   if (d->num_heads < 16 || d->num_heads > 128 || d->num_heads % 16 != 0)
     return MLA_DECODE_UNSUPPORTED;
   if (d->batch < 1 || d->batch > 65535) return MLA_DECODE_INVALID_ARG;
@@ -154,7 +154,7 @@ int check_dims(const mla_decode_dims* d) {
 // Default number of work ranges = co-resident decode CTA groups (one group =
 // the CTAs covering all query rows of a sequence).  Cached per device and
 // (q_len, heads).
-int g_groups[kMaxDevices][3][9];
+int g_groups[kMaxDevices][kMaxQLen + 1][9];
 std::mutex g_groups_mu;
 
 int default_ranges(const mla_decode_dims* d, int* R) {

@@ -36,6 +36,7 @@ constexpr int kDqk = kLora + kRope;    // 576: latent cache row, absorbed query 
 constexpr int kDq = kNope + kRope;     // 192: query row as given
 constexpr int kVHead = 128;            // output width per head
 constexpr int kPage = 64;              // tokens per cache page
+constexpr int kMaxQLen = 8;            // new query tokens per sequence (speculative drafts)
 
 // Decode tiling.
 constexpr int kTileRows = 64;          // query rows (t, h) per decode CTA

@@ -49,6 +49,8 @@ WORKLOADS = {
                      "long-context decode: B=8, L=32768, H=128"),
     "mixed_spec": Workload("mixed_spec", 256, 2, 128, 1005, ("lognormal", 800, 1.0, 32, 30000),
                            "mixed batch, q_len=2 causal pair: B=256, L~LogN(ln 800, 1) in [32,30000], H=128"),
+    "draft_q8": Workload("draft_q8", 64, 8, 128, 1006, ("lognormal", 2000, 1.0, 64, 30000),
+                         "speculative drafts, q_len=8 causal block: B=64, L~LogN(ln 2000, 1) in [64,30000], H=128"),
 }
 
 

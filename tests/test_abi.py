@@ -59,7 +59,7 @@ def good_dims(**kw):
 
 @pytest.mark.parametrize("field,value,code", [
     ("qk_nope", 64, 2), ("qk_rope", 32, 2), ("kv_lora", 256, 2), ("v_head", 64, 2),
-    ("page_size", 16, 2), ("q_len", 3, 2), ("q_len", 0, 2), ("num_heads", 8, 2),
+    ("page_size", 16, 2), ("q_len", 9, 2), ("q_len", 0, 2), ("num_heads", 8, 2),
     ("num_heads", 24, 2), ("num_heads", 256, 2), ("batch", 0, 1), ("num_pages", 0, 1),
     ("max_pages_per_seq", 0, 1),
 ])

@@ -86,13 +86,14 @@ def test_random_small_matches_explicit_form(seed):
     np.testing.assert_allclose(lse, el, rtol=1e-12, atol=1e-12)
 
 
-def test_matches_torch_sdpa_fp64_with_causal_pair():
-    inp = rand_case(7, 2, [70, 130], 2, 3)
+@pytest.mark.parametrize("T", [2, 4, 8])
+def test_matches_torch_sdpa_fp64_with_causal_block(T):
+    inp = rand_case(7 + T, 2, [70, 130], T, 3)
     out, lse, _ = oracle.decode(inp.q, inp.cache, inp.block_table, inp.seq_lens, inp.w_uk,
                                 inp.w_uv, inp.scale)
     q = inp.q.double()
     cache = inp.cache.double()
-    got = out.reshape(2, 2, 3, -1)
+    got = out.reshape(2, T, 3, -1)
     for b in range(2):
         L = int(inp.seq_lens[b])
         pages = inp.block_table[b, :(L + 63) // 64].long()
@@ -100,15 +101,17 @@ def test_matches_torch_sdpa_fp64_with_causal_pair():
         for h in range(3):
             K = torch.cat([C[:, :512] @ inp.w_uk[h].double().T, C[:, 512:]], 1)
             V = C[:, :512] @ inp.w_uv[h].double()
-            mask = torch.ones(2, L, dtype=torch.bool)
-            mask[0, L - 1] = False  # query 0 of the pair does not see the second new token
+            # query t of the block does not see the block's later new tokens
+            mask = torch.ones(T, L, dtype=torch.bool)
+            for t in range(T):
+                mask[t, L - T + t + 1:] = False
             ref = torch.nn.functional.scaled_dot_product_attention(
                 q[b, :, h][None, None], K[None, None], V[None, None], attn_mask=mask[None, None],
                 scale=inp.scale)[0, 0]
             np.testing.assert_allclose(got[b, :, h], ref.numpy(), rtol=1e-10, atol=1e-12)
             s = inp.scale * (q[b, :, h] @ K.T)
             s = s.masked_fill(~mask, float("-inf"))
-            np.testing.assert_allclose(lse.reshape(2, 2, 3)[b, :, h],
+            np.testing.assert_allclose(lse.reshape(2, T, 3)[b, :, h],
                                        torch.logsumexp(s, dim=1).numpy(), rtol=1e-12)
 
 

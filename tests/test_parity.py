@@ -50,7 +50,8 @@ def test_tiny_workload_all_rows():
 # 48/80 heads leave a partial last tile; 96 x 2 rows make three tiles; 112 x 2
 # rows make four with a 32-row last tile.
 @pytest.mark.parametrize("H,T", [(16, 1), (32, 1), (64, 1), (128, 1), (16, 2), (64, 2), (128, 2),
-                                 (48, 1), (80, 1), (96, 2), (112, 2)])
+                                 (48, 1), (80, 1), (96, 2), (112, 2),
+                                 (16, 4), (128, 3), (64, 8), (128, 8)])
 def test_ragged_lengths_all_rows(H, T):
     lens = [T, 1 + T, 63, 64, 65, 127, 128, 129, 200, 511, 700]
     inp = make_inputs(len(lens), lens, T, H, seed=100 + H + T)
@@ -66,6 +67,15 @@ def test_split_counts(num_ranges):
     hdr = m.plan_header()
     assert hdr[0] == num_ranges
     assert_parity(compare(inp, out, lse), "R=%d" % num_ranges)
+
+
+@pytest.mark.parametrize("num_ranges", [1, 7, 40])
+def test_split_counts_long_drafts(num_ranges):
+    # q_len 8: query t of the draft sees keys [0, L - 8 + t]
+    lens = [8, 9, 600, 1500, 77]
+    inp = make_inputs(len(lens), lens, 8, 32, seed=17)
+    out, lse, _ = run_gpu(inp, num_ranges=num_ranges)
+    assert_parity(compare(inp, out, lse), "T=8 R=%d" % num_ranges)
 
 
 def test_split_counts_h128():
@@ -208,7 +218,7 @@ def test_late_pages_force_rescale(H, T, R):
     assert_parity(compare(inp, out, lse), "H=%d T=%d R=%d" % (H, T, R))
 
 
-@pytest.mark.parametrize("name", ["tp_shard", "full_head", "long", "mixed_spec"])
+@pytest.mark.parametrize("name", ["tp_shard", "full_head", "long", "mixed_spec", "draft_q8"])
 def test_full_size_workloads_sampled(name):
     inp = workload_inputs(name)
     out, lse, _ = run_gpu(inp)
