@@ -146,6 +146,30 @@ int mla_decode_combine(const mla_decode_dims* dims, float softmax_scale, float* 
 int mla_decode_up_project(const mla_decode_dims* dims, const void* w_uv, void* out,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same steps with FP8 weights.  The page says the absorbed form has no FP8
+ * bmm, so the weights are decompressed to bf16 and the bmm runs in bf16; here
+ * the bmm kernels decompress each weight tile as they load it.
+ *   w_uk_fp8    uint8 [H, 128, 512]  FP8 E4M3 (4-bit exponent, bias 7, 3-bit
+ *               mantissa, no infinities; S.1111.111 is NaN)
+ *   w_uk_scale  fp32  [H, 1, 4]      one scale per 128 x 128 block (k, m)
+ *   w_uv_fp8    uint8 [H, 512, 128]  FP8 E4M3
+ *   w_uv_scale  fp32  [H, 4, 1]
+ * The weight used is W = bf16(fp32(w8) * scale): the fp32 product rounded to
+ * the nearest bf16 (ties to even).  Pointers as for the bf16 calls; the FP8
+ * arrays need 16-byte alignment, the scales 4-byte alignment. */
+int mla_decode_run_fp8w(const mla_decode_dims* dims, const void* q, const void* kv_cache,
+                        const int32_t* block_table, const int32_t* seq_lens,
+                        const uint8_t* w_uk_fp8, const float* w_uk_scale,
+                        const uint8_t* w_uv_fp8, const float* w_uv_scale, float softmax_scale,
+                        void* out, float* lse, void* workspace, size_t workspace_bytes,
+                        void* stream);
+int mla_decode_absorb_fp8w(const mla_decode_dims* dims, const void* q, const uint8_t* w_uk_fp8,
+                           const float* w_uk_scale, void* workspace, size_t workspace_bytes,
+                           void* stream);
+int mla_decode_up_project_fp8w(const mla_decode_dims* dims, const uint8_t* w_uv_fp8,
+                               const float* w_uv_scale, void* out, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
 /* Waits for `stream`, then returns the first device-side status recorded in
  * the workspace since the last plan (OK, DEVICE_BOUNDS or TIMEOUT), or
  * CUDA_ERROR if the stream reports an error. */

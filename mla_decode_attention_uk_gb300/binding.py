@@ -23,7 +23,8 @@ ENTRY_POINTS = (
     "mla_decode_plan_ex", "mla_decode_run", "mla_decode_absorb", "mla_decode_attend",
     "mla_decode_combine", "mla_decode_up_project", "mla_decode_check", "mla_decode_status_string",
     "mla_decode_workspace_offsets", "mla_decode_kernels_per_run",
-    "mla_decode_run_static_scratch", "mla_decode_selftest_wait_timeout")
+    "mla_decode_run_static_scratch", "mla_decode_selftest_wait_timeout",
+    "mla_decode_run_fp8w", "mla_decode_absorb_fp8w", "mla_decode_up_project_fp8w")
 
 
 class Dims(ctypes.Structure):
@@ -67,6 +68,9 @@ def lib():
         L.mla_decode_workspace_offsets.argtypes = [D, i32, ctypes.POINTER(ctypes.c_int64), i32]
         L.mla_decode_run_static_scratch.argtypes = [D, P, P, P, P, P, P, ctypes.c_float, P, P, P]
         L.mla_decode_selftest_wait_timeout.argtypes = [P, P]
+        L.mla_decode_run_fp8w.argtypes = [D, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, S, P]
+        L.mla_decode_absorb_fp8w.argtypes = [D, P, P, P, P, S, P]
+        L.mla_decode_up_project_fp8w.argtypes = [D, P, P, P, P, S, P]
         for n in ENTRY_POINTS:
             if n != "mla_decode_status_string":
                 getattr(L, n).restype = ctypes.c_int
@@ -128,6 +132,27 @@ class MlaDecode:
                                  _ptr(seq_lens), _ptr(w_uk), _ptr(w_uv), float(scale), _ptr(out),
                                  _ptr(lse), _ptr(self.workspace), self.ws_bytes, _stream()),
             "mla_decode_run")
+
+    def run_fp8w(self, q, cache, block_table, seq_lens, w_uk8, w_uk_scale, w_uv8, w_uv_scale,
+                 scale, out, lse):
+        _ok(lib().mla_decode_run_fp8w(ctypes.byref(self.dims), _ptr(q), _ptr(cache),
+                                      _ptr(block_table), _ptr(seq_lens), _ptr(w_uk8),
+                                      _ptr(w_uk_scale), _ptr(w_uv8), _ptr(w_uv_scale),
+                                      float(scale), _ptr(out), _ptr(lse), _ptr(self.workspace),
+                                      self.ws_bytes, _stream()),
+            "mla_decode_run_fp8w")
+
+    def absorb_fp8w(self, q, w_uk8, w_uk_scale):
+        _ok(lib().mla_decode_absorb_fp8w(ctypes.byref(self.dims), _ptr(q), _ptr(w_uk8),
+                                         _ptr(w_uk_scale), _ptr(self.workspace), self.ws_bytes,
+                                         _stream()),
+            "mla_decode_absorb_fp8w")
+
+    def up_project_fp8w(self, w_uv8, w_uv_scale, out):
+        _ok(lib().mla_decode_up_project_fp8w(ctypes.byref(self.dims), _ptr(w_uv8),
+                                             _ptr(w_uv_scale), _ptr(out), _ptr(self.workspace),
+                                             self.ws_bytes, _stream()),
+            "mla_decode_up_project_fp8w")
 
     def absorb(self, q, w_uk):
         _ok(lib().mla_decode_absorb(ctypes.byref(self.dims), _ptr(q), _ptr(w_uk),

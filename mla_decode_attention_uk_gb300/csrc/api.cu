@@ -20,9 +20,11 @@ cudaError_t launch_plan(const int32_t* seq_lens, int B, int T, int max_pages, in
 int bmm_token_tile(int BT);
 cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q, int BT, int H,
                           const __nv_bfloat16* q, __nv_bfloat16* qlat, __nv_bfloat16* qlo,
-                          int32_t* status, cudaStream_t st);
+                          int32_t* status, cudaStream_t st, const uint8_t* wuk8,
+                          const float* wuk_scale);
 cudaError_t launch_up_project(const CUtensorMap& tm_wuv, const CUtensorMap& tm_olat, int BT,
-                              int H, __nv_bfloat16* out, int32_t* status, cudaStream_t st);
+                              int H, __nv_bfloat16* out, int32_t* status, cudaStream_t st,
+                              const uint8_t* wuv8, const float* wuv_scale);
 int decode_tiles(int T, int H);
 int decode_q_box_rows(int T, int H);
 cudaError_t decode_max_groups(int T, int H, int sm_count, int* groups);
@@ -264,11 +266,16 @@ int mla_decode_plan(const mla_decode_dims* d, const int32_t* seq_lens, void* ws,
   return mla_decode_plan_ex(d, seq_lens, 0, ws, ws_bytes, stream);
 }
 
-int mla_decode_absorb(const mla_decode_dims* d, const void* q, const void* w_uk, void* ws,
-                      size_t ws_bytes, void* stream) {
+// Steps a2 and a5 with bf16 weights (w_*) or FP8 weights (w8_* with block
+// scales); exactly one of the two is given.
+static int absorb_impl(const mla_decode_dims* d, const void* q, const void* w_uk,
+                       const uint8_t* w8, const float* w8_scale, void* ws, size_t ws_bytes,
+                       void* stream) {
   int rc = check_dims(d);
   if (rc) return rc;
-  if (!q || !w_uk || !ws || !aligned16(q) || !aligned16(w_uk) || !aligned16(ws))
+  const void* w = w8 ? static_cast<const void*>(w8) : w_uk;
+  if (!q || !w || !ws || !aligned16(q) || !aligned16(w) || !aligned16(ws) ||
+      (w8 && (!w8_scale || (reinterpret_cast<uintptr_t>(w8_scale) & 3u))))
     return MLA_DECODE_INVALID_ARG;
   WsLayout L;
   rc = layout_for(d, ws_bytes, &L);
@@ -276,12 +283,56 @@ int mla_decode_absorb(const mla_decode_dims* d, const void* q, const void* w_uk,
   const int BT = d->batch * d->q_len, H = d->num_heads;
   CUtensorMap tm_q, tm_w;
   if (!make_map(&tm_q, q, BT, static_cast<uint64_t>(H) * kDq, static_cast<uint64_t>(H) * kDq,
-                kBoxCols, bmm_token_tile(BT), false) ||
-      !make_map(&tm_w, w_uk, static_cast<uint64_t>(H) * kNope, kLora, kLora, kBoxCols, 64, false))
+                kBoxCols, bmm_token_tile(BT), false))
+    return MLA_DECODE_CUDA_ERROR;
+  if (w8)
+    tm_w = tm_q;  // not read: the kernel converts the FP8 weights itself
+  else if (!make_map(&tm_w, w_uk, static_cast<uint64_t>(H) * kNope, kLora, kLora, kBoxCols, 64,
+                     false))
     return MLA_DECODE_CUDA_ERROR;
   return cuda_rc(launch_absorb(tm_w, tm_q, BT, H, static_cast<const __nv_bfloat16*>(q),
                                at<__nv_bfloat16>(ws, L.qlat), at<__nv_bfloat16>(ws, L.qlo),
-                               at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream)));
+                               at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream), w8,
+                               w8_scale));
+}
+
+static int up_project_impl(const mla_decode_dims* d, const void* w_uv, const uint8_t* w8,
+                           const float* w8_scale, void* out, void* ws, size_t ws_bytes,
+                           void* stream) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  const void* w = w8 ? static_cast<const void*>(w8) : w_uv;
+  if (!w || !out || !ws || !aligned16(w) || !aligned16(out) || !aligned16(ws) ||
+      (w8 && (!w8_scale || (reinterpret_cast<uintptr_t>(w8_scale) & 3u))))
+    return MLA_DECODE_INVALID_ARG;
+  WsLayout L;
+  rc = layout_for(d, ws_bytes, &L);
+  if (rc) return rc;
+  const int BT = d->batch * d->q_len, H = d->num_heads;
+  CUtensorMap tm_o, tm_w;
+  if (!make_map(&tm_o, at<void>(ws, L.olat), BT, static_cast<uint64_t>(H) * kLora,
+                static_cast<uint64_t>(H) * kLora, kBoxCols, bmm_token_tile(BT), false))
+    return MLA_DECODE_CUDA_ERROR;
+  if (w8)
+    tm_w = tm_o;  // not read: the kernel converts the FP8 weights itself
+  else if (!make_map(&tm_w, w_uv, static_cast<uint64_t>(H) * kLora, kVHead, kVHead, kBoxCols, 64,
+                     false))
+    return MLA_DECODE_CUDA_ERROR;
+  return cuda_rc(launch_up_project(tm_w, tm_o, BT, H, static_cast<__nv_bfloat16*>(out),
+                                   at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream),
+                                   w8, w8_scale));
+}
+
+int mla_decode_absorb(const mla_decode_dims* d, const void* q, const void* w_uk, void* ws,
+                      size_t ws_bytes, void* stream) {
+  if (!w_uk) return MLA_DECODE_INVALID_ARG;
+  return absorb_impl(d, q, w_uk, nullptr, nullptr, ws, ws_bytes, stream);
+}
+
+int mla_decode_absorb_fp8w(const mla_decode_dims* d, const void* q, const uint8_t* w_uk_fp8,
+                           const float* w_uk_scale, void* ws, size_t ws_bytes, void* stream) {
+  if (!w_uk_fp8) return MLA_DECODE_INVALID_ARG;
+  return absorb_impl(d, q, nullptr, w_uk_fp8, w_uk_scale, ws, ws_bytes, stream);
 }
 
 int mla_decode_attend(const mla_decode_dims* d, const void* kv_cache, const int32_t* block_table,
@@ -332,22 +383,15 @@ int mla_decode_combine(const mla_decode_dims* d, float scale, float* lse, void* 
 
 int mla_decode_up_project(const mla_decode_dims* d, const void* w_uv, void* out, void* ws,
                           size_t ws_bytes, void* stream) {
-  int rc = check_dims(d);
-  if (rc) return rc;
-  if (!w_uv || !out || !ws || !aligned16(w_uv) || !aligned16(out) || !aligned16(ws))
-    return MLA_DECODE_INVALID_ARG;
-  WsLayout L;
-  rc = layout_for(d, ws_bytes, &L);
-  if (rc) return rc;
-  const int BT = d->batch * d->q_len, H = d->num_heads;
-  CUtensorMap tm_o, tm_w;
-  if (!make_map(&tm_o, at<void>(ws, L.olat), BT, static_cast<uint64_t>(H) * kLora,
-                static_cast<uint64_t>(H) * kLora, kBoxCols, bmm_token_tile(BT), false) ||
-      !make_map(&tm_w, w_uv, static_cast<uint64_t>(H) * kLora, kVHead, kVHead, kBoxCols, 64,
-                false))
-    return MLA_DECODE_CUDA_ERROR;
-  return cuda_rc(launch_up_project(tm_w, tm_o, BT, H, static_cast<__nv_bfloat16*>(out),
-                                   at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream)));
+  if (!w_uv) return MLA_DECODE_INVALID_ARG;
+  return up_project_impl(d, w_uv, nullptr, nullptr, out, ws, ws_bytes, stream);
+}
+
+int mla_decode_up_project_fp8w(const mla_decode_dims* d, const uint8_t* w_uv_fp8,
+                               const float* w_uv_scale, void* out, void* ws, size_t ws_bytes,
+                               void* stream) {
+  if (!w_uv_fp8) return MLA_DECODE_INVALID_ARG;
+  return up_project_impl(d, nullptr, w_uv_fp8, w_uv_scale, out, ws, ws_bytes, stream);
 }
 
 int mla_decode_run(const mla_decode_dims* d, const void* q, const void* kv_cache,
@@ -361,6 +405,20 @@ int mla_decode_run(const mla_decode_dims* d, const void* q, const void* kv_cache
   rc = mla_decode_combine(d, scale, lse, ws, ws_bytes, stream);
   if (rc) return rc;
   return mla_decode_up_project(d, w_uv, out, ws, ws_bytes, stream);
+}
+
+int mla_decode_run_fp8w(const mla_decode_dims* d, const void* q, const void* kv_cache,
+                        const int32_t* block_table, const int32_t* seq_lens,
+                        const uint8_t* w_uk_fp8, const float* w_uk_scale,
+                        const uint8_t* w_uv_fp8, const float* w_uv_scale, float scale, void* out,
+                        float* lse, void* ws, size_t ws_bytes, void* stream) {
+  int rc = mla_decode_absorb_fp8w(d, q, w_uk_fp8, w_uk_scale, ws, ws_bytes, stream);
+  if (rc) return rc;
+  rc = mla_decode_attend(d, kv_cache, block_table, seq_lens, scale, lse, ws, ws_bytes, stream);
+  if (rc) return rc;
+  rc = mla_decode_combine(d, scale, lse, ws, ws_bytes, stream);
+  if (rc) return rc;
+  return mla_decode_up_project_fp8w(d, w_uv_fp8, w_uv_scale, out, ws, ws_bytes, stream);
 }
 
 int mla_decode_workspace_offsets(const mla_decode_dims* d, int32_t num_ranges,

@@ -17,8 +17,18 @@
 //
 // The absorb epilogue also writes the bf16 residual q_lat - bf16(q_lat), which
 // the attention step uses to correct its log-sum-exp to first order.
+//
+// FP8 weights (W8): the page says the absorbed form lacks an FP8 bmm, so the
+// matrices involved are decompressed to bf16 and the bmm runs in bf16.  Here
+// the decompression happens inside the bmm: W is stored as FP8 E4M3 with one
+// fp32 scale per 128 x 128 block, warps 2-3 load each stage's 64 x 128 FP8
+// tile, form W = bf16(fp32(w8) * scale) (fp32 product, round to nearest even)
+// and write it straight into the swizzled shared-memory layout the MMA reads,
+// while warp 0 brings the activation tile by TMA.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -33,6 +43,13 @@ constexpr int kABytes = 2 * kBoxBytes;  // 128 m x 64 k, two 64-wide m boxes
 
 enum class BmmMode { kAbsorb, kUpProject };
 
+// FP8 weights: E4M3 bytes [H, K, M] and fp32 scales [H, K/128, M/128].
+struct Fp8Weights {
+  const uint8_t* w;
+  const float* scale;
+  int M;
+};
+
 template <int NT, int STAGES>
 struct BmmSmem {
   static constexpr int kBBytes = NT * 128;
@@ -43,12 +60,12 @@ struct BmmSmem {
   static constexpr int kTotal = kBody + 1024;  // + alignment slack
 };
 
-template <BmmMode MODE, int NT, int STAGES>
+template <BmmMode MODE, int NT, int STAGES, bool W8>
 __global__ void __launch_bounds__(kBmmThreads)
 bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
            int BT, int H, int K, int Kx, const __nv_bfloat16* __restrict__ q,
            __nv_bfloat16* __restrict__ out_hi, __nv_bfloat16* __restrict__ out_lo,
-           int32_t* __restrict__ status) {
+           int32_t* __restrict__ status, Fp8Weights w8) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], done_bar;
   __shared__ uint32_t tmem_base_sh;
@@ -73,13 +90,14 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&full_bar[s]), 1);
+      // FP8 weights: the TMA transaction and the converters' arrival.
+      mbar_init(smem_u32(&full_bar[s]), W8 ? 2 : 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     mbar_init(smem_u32(&done_bar), 1);
     abort_sh = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&tm_w);
+    if (!W8) tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_x);
   }
   if (warp == 2) {
@@ -99,9 +117,11 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
         for (int kc = 0; kc < kc0; ++kc) {
           const uint32_t a = sbase + kc * S::kStageBytes;
           const uint32_t fb = smem_u32(&full_bar[kc]);
-          mbar_expect_tx(fb, S::kStageBytes);
-          tma_load_2d(a, &tm_w, m0, h * K + kc * 64, fb);
-          tma_load_2d(a + kBoxBytes, &tm_w, m0 + 64, h * K + kc * 64, fb);
+          mbar_expect_tx(fb, W8 ? S::kBBytes : S::kStageBytes);
+          if (!W8) {
+            tma_load_2d(a, &tm_w, m0, h * K + kc * 64, fb);
+            tma_load_2d(a + kBoxBytes, &tm_w, m0 + 64, h * K + kc * 64, fb);
+          }
         }
         griddep_wait();  // o_lat comes from the step before
         for (int kc = 0; kc < kc0; ++kc) {
@@ -117,11 +137,52 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
         const uint32_t a = sbase + s * S::kStageBytes;
         const uint32_t b = a + kABytes;
         const uint32_t fb = smem_u32(&full_bar[s]);
-        mbar_expect_tx(fb, S::kStageBytes);
-        tma_load_2d(a, &tm_w, m0, h * K + kc * 64, fb);
-        tma_load_2d(a + kBoxBytes, &tm_w, m0 + 64, h * K + kc * 64, fb);
+        mbar_expect_tx(fb, W8 ? S::kBBytes : S::kStageBytes);
+        if (!W8) {
+          tma_load_2d(a, &tm_w, m0, h * K + kc * 64, fb);
+          tma_load_2d(a + kBoxBytes, &tm_w, m0 + 64, h * K + kc * 64, fb);
+        }
         tma_load_2d(b, &tm_x, h * Kx + kc * 64, tok0, fb);
       }
+    }
+  } else if (W8 && warp >= 2) {
+    // FP8 weight converters: thread kr (0..63) owns k row kr of each stage's
+    // 64 x 128 weight tile.  The tile's bf16 layout is the one TMA would have
+    // produced: two 64-column m boxes, 128-byte rows, 16-byte chunks swizzled
+    // by the row index (128B swizzle).
+    const int kr = threadIdx.x - 64;
+    for (int kc = 0; kc < nk; ++kc) {
+      const int s = kc % STAGES;
+      if (kc >= STAGES &&
+          !mbar_wait(smem_u32(&empty_bar[s]), ((kc / STAGES) - 1) & 1, &abort_sh, status))
+        break;
+      const uint32_t a = sbase + s * S::kStageBytes;
+      const size_t krow = static_cast<size_t>(h) * K + kc * 64 + kr;
+      const uint4* src = reinterpret_cast<const uint4*>(w8.w + krow * w8.M + m0);
+      const float sc =
+          __ldg(w8.scale + (static_cast<size_t>(h) * (K / 128) + (kc * 64) / 128) * (w8.M / 128) +
+                m0 / 128);
+#pragma unroll
+      for (int qd = 0; qd < 8; ++qd) {  // 16 weights (m) per 16-byte load
+        const uint4 raw = __ldg(src + qd);
+        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t ow[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {  // two E4M3 values -> one bf16 pair
+          const __nv_fp8x2_storage_t pr =
+              static_cast<__nv_fp8x2_storage_t>((rw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+          const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
+          const __nv_bfloat162 bv = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+          ow[e] = *reinterpret_cast<const uint32_t*>(&bv);
+        }
+        const int box = qd >> 2, c0 = 2 * (qd & 3);
+        const uint32_t row = a + box * kBoxBytes + kr * 128;
+        st_shared_v4(row + ((c0 ^ (kr & 7)) << 4), ow[0], ow[1], ow[2], ow[3]);
+        st_shared_v4(row + (((c0 + 1) ^ (kr & 7)) << 4), ow[4], ow[5], ow[6], ow[7]);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 64);
+      if (kr == 0) mbar_arrive(smem_u32(&full_bar[s]));
     }
   } else if (warp == 1) {
     if (elect_one()) {
@@ -211,17 +272,18 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
 template <BmmMode MODE, int NT>
 cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, int H, int K,
                           int Kx, int Mtot, const __nv_bfloat16* q, __nv_bfloat16* hi,
-                          __nv_bfloat16* lo, int32_t* status, cudaStream_t st) {
+                          __nv_bfloat16* lo, int32_t* status, cudaStream_t st,
+                          Fp8Weights w8) {
   // Two stages for the absorb step (K = 128) and for 128-token tiles (64 KB of
   // stages, three CTAs per SM); four for the up-projection's smaller tiles.
   constexpr int STAGES = (MODE == BmmMode::kAbsorb || NT == 128) ? 2 : 4;
-  auto kern = bmm_kernel<MODE, NT, STAGES>;
+  auto kern = w8.w ? bmm_kernel<MODE, NT, STAGES, true> : bmm_kernel<MODE, NT, STAGES, false>;
   const int smem = BmmSmem<NT, STAGES>::kTotal;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((BT + NT - 1) / NT, Mtot / 128, H);
   e = launch_pdl(kern, grid, dim3(kBmmThreads), smem, st, tw, tx, BT, H, K, Kx, q, hi, lo,
-                 status);
+                 status, w8);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -238,22 +300,26 @@ int bmm_token_tile(int BT) {
 
 cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q, int BT, int H,
                           const __nv_bfloat16* q, __nv_bfloat16* qlat, __nv_bfloat16* qlo,
-                          int32_t* status, cudaStream_t st) {
+                          int32_t* status, cudaStream_t st, const uint8_t* wuk8,
+                          const float* wuk_scale) {
+  const Fp8Weights w8{wuk8, wuk_scale, kLora};
   switch (bmm_token_tile(BT)) {
-    case 16: return launch_bmm_nt<BmmMode::kAbsorb, 16>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st);
-    case 32: return launch_bmm_nt<BmmMode::kAbsorb, 32>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st);
-    case 64: return launch_bmm_nt<BmmMode::kAbsorb, 64>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st);
-    default: return launch_bmm_nt<BmmMode::kAbsorb, 128>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st);
+    case 16: return launch_bmm_nt<BmmMode::kAbsorb, 16>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st, w8);
+    case 32: return launch_bmm_nt<BmmMode::kAbsorb, 32>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st, w8);
+    case 64: return launch_bmm_nt<BmmMode::kAbsorb, 64>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st, w8);
+    default: return launch_bmm_nt<BmmMode::kAbsorb, 128>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st, w8);
   }
 }
 
 cudaError_t launch_up_project(const CUtensorMap& tm_wuv, const CUtensorMap& tm_olat, int BT,
-                              int H, __nv_bfloat16* out, int32_t* status, cudaStream_t st) {
+                              int H, __nv_bfloat16* out, int32_t* status, cudaStream_t st,
+                              const uint8_t* wuv8, const float* wuv_scale) {
+  const Fp8Weights w8{wuv8, wuv_scale, kVHead};
   switch (bmm_token_tile(BT)) {
-    case 16: return launch_bmm_nt<BmmMode::kUpProject, 16>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st);
-    case 32: return launch_bmm_nt<BmmMode::kUpProject, 32>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st);
-    case 64: return launch_bmm_nt<BmmMode::kUpProject, 64>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st);
-    default: return launch_bmm_nt<BmmMode::kUpProject, 128>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st);
+    case 16: return launch_bmm_nt<BmmMode::kUpProject, 16>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);
+    case 32: return launch_bmm_nt<BmmMode::kUpProject, 32>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);
+    case 64: return launch_bmm_nt<BmmMode::kUpProject, 64>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);
+    default: return launch_bmm_nt<BmmMode::kUpProject, 128>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);
   }
 }
 

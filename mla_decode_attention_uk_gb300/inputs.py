@@ -148,3 +148,19 @@ def workload_seq_lens(name: str) -> List[int]:
     w = WORKLOADS[name]
     g = torch.Generator().manual_seed(w.seed)
     return draw_seq_lens(w, g)
+
+
+def quantize_fp8_blockwise(w):
+    """FP8 E4M3 weights with one fp32 scale per 128 x 128 block of each head's
+    [K, M] matrix: scale = block amax / 448, codes = E4M3(w / scale).  Input
+    preparation for the FP8-weight path (the decompression is the method's
+    step and lives in the kernels and the oracle).  Returns (uint8 [H, K, M],
+    fp32 [H, K/128, M/128])."""
+    H, K, M = w.shape
+    wf = w.to(torch.float32).reshape(H, K // 128, 128, M // 128, 128)
+    amax = wf.abs().amax(dim=(2, 4))
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = (wf / scale[:, :, None, :, None]).reshape(H, K, M)
+    codes = q.to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.contiguous(), scale.contiguous()
+

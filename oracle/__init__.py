@@ -136,3 +136,37 @@ def up_project(w_uv, h, o_lat):
 
 def default_scale(qk_nope=128, qk_rope=64):
     return 1.0 / math.sqrt(qk_nope + qk_rope)
+
+
+# ---------------------------------------------------------------------------
+# FP8 weights.  vLLM PR #14770 (PR description): without an FP8 bmm the
+# matrices involved in the bmm are decompressed to bf16 and the bmm runs in
+# bf16.  The decompression follows the FP8 E4M3 encoding and one fp32 scale per
+# 128 x 128 block (k, m) of each head's matrix; the decompressed weight is the
+# fp32 product rounded to the nearest bf16 (ties to even).  The bf16 oracle
+# above then applies unchanged.
+
+def e4m3_to_float(codes):
+    """Values of FP8 E4M3 codes (uint8 array): sign bit, 4-bit exponent with
+    bias 7, 3-bit mantissa; exponent 0 is subnormal (m/8 * 2^-6); no
+    infinities; S.1111.111 is NaN.  Returns float64."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    normal = sign * (1.0 + m / 8.0) * np.exp2(e - 7.0)
+    sub = sign * (m / 8.0) * 2.0 ** -6
+    v = np.where(e == 0, sub, normal)
+    return np.where((e == 0xF) & (m == 0x7), np.nan, v)
+
+
+def dequant_fp8_weight(w8, scale):
+    """bf16 weight [H, K, M] from E4M3 codes w8 (uint8 [H, K, M]) and fp32 block
+    scales [H, K/128, M/128]: bf16(fp32(value) * fp32(scale))."""
+    w8 = torch.as_tensor(w8)
+    H, K, M = w8.shape
+    vals = torch.from_numpy(e4m3_to_float(w8.numpy()).astype(np.float32))  # exact in fp32
+    s = scale.to(torch.float32).repeat_interleave(128, 1).repeat_interleave(128, 2)
+    assert s.shape == (H, K, M)
+    return (vals * s).to(torch.bfloat16)  # fp32 product, then round to nearest even
+

@@ -388,3 +388,40 @@ def test_planted_mistake_fails_a_pin(name, mutant_dir):
     caught = rc != 0 or not (np.allclose(out, eo, rtol=1e-9, atol=1e-11)
                              and np.allclose(lse, el, rtol=1e-11, atol=1e-11))
     assert caught, "planted mistake %s went unnoticed" % name
+
+
+# ---------------------------------------------------------------------------
+# FP8 weights: E4M3 decoding and the bf16 decompression rule.
+
+def test_e4m3_decoding_matches_torch_float8_for_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_to_float(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+    assert np.array_equal(np.signbit(mine[ok]), np.signbit(ref[ok]))
+
+
+def test_e4m3_known_values():
+    v = oracle.e4m3_to_float(np.array([0x00, 0x38, 0x40, 0x7E, 0x01, 0x08, 0xB8, 0x80, 0x7F, 0xFF],
+                                      dtype=np.uint8))
+    assert list(v[:7]) == [0.0, 1.0, 2.0, 448.0, 2.0 ** -9, 2.0 ** -6, -1.0]
+    assert v[7] == 0.0 and np.signbit(v[7])
+    assert np.isnan(v[8]) and np.isnan(v[9])
+
+
+def test_fp8_dequant_rounds_to_nearest_even_bf16_and_uses_block_scales():
+    # Code 0x38 is 1.0.  With scale 1 + 2^-8 the product lies exactly halfway
+    # between the bf16 neighbours 1 and 1 + 2^-7: ties go to the even one, 1.
+    # With 1 + 3 * 2^-8 it lies halfway between 1 + 2^-7 and 1 + 2^-6: 1 + 2^-6.
+    w8 = torch.full((1, 128, 256), 0x38, dtype=torch.uint8)
+    scale = torch.tensor([[[1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8]]], dtype=torch.float32)
+    d = oracle.dequant_fp8_weight(w8, scale).double()
+    assert torch.all(d[0, :, :128] == 1.0) and torch.all(d[0, :, 128:] == 1 + 2.0 ** -6)
+    # Each 128 x 128 block takes its own scale.
+    w8 = torch.full((2, 256, 128), 0x38, dtype=torch.uint8)
+    scale = torch.tensor([[[2.0], [4.0]], [[8.0], [0.5]]], dtype=torch.float32)
+    d = oracle.dequant_fp8_weight(w8, scale).double()
+    assert torch.all(d[0, :128] == 2.0) and torch.all(d[0, 128:] == 4.0)
+    assert torch.all(d[1, :128] == 8.0) and torch.all(d[1, 128:] == 0.5)

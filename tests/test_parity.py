@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from mla_decode_attention_uk_gb300 import binding
-from mla_decode_attention_uk_gb300.inputs import make_inputs, workload_inputs
+from mla_decode_attention_uk_gb300.inputs import make_inputs, quantize_fp8_blockwise, workload_inputs
 
 from parity_util import assert_parity, compare, run_gpu, sample_rows
 
@@ -225,3 +225,32 @@ def test_full_size_workloads_sampled(name):
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
     rows = sample_rows(inp, 96, seed=1)
     assert_parity(compare(inp, out, lse, rows=rows), name)
+
+
+@pytest.mark.parametrize("B,T,H", [(3, 1, 16), (20, 1, 64), (40, 2, 128)])
+def test_fp8_weights_equal_bf16_run_on_decompressed_weights(B, T, H):
+    # 16-, 32- and 128-token bmm tiles.  The kernels decompress each FP8 weight
+    # tile to bf16 as they load it; the result must equal, bit for bit, the bf16
+    # path given the weights the oracle decompresses, and match the oracle.
+    g = torch.Generator().manual_seed(60 + H)
+    lens = torch.randint(T, 900, (B,), generator=g).tolist()
+    inp = make_inputs(B, lens, T, H, seed=61 + H)
+    uk8, uk_s = quantize_fp8_blockwise(inp.w_uk)
+    uv8, uv_s = quantize_fp8_blockwise(inp.w_uv)
+    inp.w_uk = oracle.dequant_fp8_weight(uk8, uk_s)
+    inp.w_uv = oracle.dequant_fp8_weight(uv8, uv_s)
+    dev = torch.device("cuda")
+    gd = inp.to(dev)
+    d = binding.dims_for(gd.q, gd.cache, gd.block_table)
+    m = binding.MlaDecode(d, dev)
+    o8 = torch.empty(B, T, H, 128, dtype=torch.bfloat16, device=dev)
+    l8 = torch.empty(B, T, H, dtype=torch.float32, device=dev)
+    ob, lb = torch.empty_like(o8), torch.empty_like(l8)
+    m.plan(gd.seq_lens)
+    m.run_fp8w(gd.q, gd.cache, gd.block_table, gd.seq_lens, uk8.to(dev), uk_s.to(dev),
+               uv8.to(dev), uv_s.to(dev), gd.scale, o8, l8)
+    m.run(gd.q, gd.cache, gd.block_table, gd.seq_lens, gd.w_uk, gd.w_uv, gd.scale, ob, lb)
+    assert m.check() == 0
+    assert torch.equal(o8, ob) and torch.equal(l8, lb)
+    assert_parity(compare(inp, o8.cpu(), l8.cpu()), "fp8 weights B=%d T=%d H=%d" % (B, T, H))
+
