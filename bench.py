@@ -12,6 +12,10 @@ HBM copy bandwidth, an end-to-end figure through the same C ABI with host
 buffers, and the fp64 CPU oracle timed on a bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+                  [--weights bf16|fp8]
+
+--weights fp8 gives the two bmms W_UK and W_UV as FP8 E4M3 codes with one
+fp32 scale per 128 x 128 block (decompressed to bf16 inside the bmm kernels).
 
 N > 1 runs under torch.distributed.run, one independent replica per GPU
 (the path needs no exchange between GPUs: weak scaling).
@@ -71,7 +75,7 @@ def ncu_traffic(workload):
     return e.get("dram_bytes_per_launch")
 
 
-def workload_stats(inp):
+def workload_stats(inp, fp8_weights=False):
     B, T, H = inp.q.shape[:3]
     sum_len = int(inp.seq_lens.sum())
     rows_keys = 0
@@ -80,6 +84,8 @@ def workload_stats(inp):
             rows_keys += H * (L - T + t + 1)
     cache_bytes = BYTES_PER_TOKEN * sum_len
     weight_bytes = H * 2 * (128 * 512 * 2)
+    if fp8_weights:  # one byte per weight plus one fp32 scale per 128 x 128 block
+        weight_bytes = H * 2 * (128 * 512 + 4 * 4)
     flops = FLOP_PER_ROW_KEY * rows_keys + FLOP_PER_ROW_BMM * B * T * H
     return dict(B=B, T=T, H=H, sum_len=sum_len, cache_bytes=cache_bytes,
                 weight_bytes=weight_bytes, flops=flops, attn_flops=FLOP_PER_ROW_KEY * rows_keys,
@@ -275,6 +281,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch every step from the host")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"],
+                    help="W_UK / W_UV as bf16, or FP8 E4M3 with 128x128 block scales")
     ap.add_argument("--breakdown", action="store_true",
                     help="also time each step of the path alone (graph replays)")
     args = ap.parse_args()
@@ -290,8 +298,38 @@ def main():
     stream = torch.cuda.current_stream()
 
     inp_cpu = workload_inputs(args.workload)
-    stats = workload_stats(inp_cpu)
+    fp8 = args.weights == "fp8"
+    stats = workload_stats(inp_cpu, fp8)
     g = inp_cpu.to(dev)
+    # Weight operands of the two bmms: name -> (host tensor, device tensor).
+    if fp8:
+        from mla_decode_attention_uk_gb300.inputs import quantize_fp8_blockwise
+        uk8, uk_s = quantize_fp8_blockwise(inp_cpu.w_uk)
+        uv8, uv_s = quantize_fp8_blockwise(inp_cpu.w_uv)
+        wts = {k: (t, t.to(dev)) for k, t in (("uk8", uk8), ("uk_s", uk_s), ("uv8", uv8),
+                                              ("uv_s", uv_s))}
+    else:
+        wts = {"w_uk": (inp_cpu.w_uk, g.w_uk), "w_uv": (inp_cpu.w_uv, g.w_uv)}
+    W = {k: v[1] for k, v in wts.items()}
+
+    def absorb():
+        if fp8:
+            m.absorb_fp8w(g.q, W["uk8"], W["uk_s"])
+        else:
+            m.absorb(g.q, W["w_uk"])
+
+    def up_project():
+        if fp8:
+            m.up_project_fp8w(W["uv8"], W["uv_s"], out)
+        else:
+            m.up_project(W["w_uv"], out)
+
+    def run_all():
+        if fp8:
+            m.run_fp8w(g.q, g.cache, g.block_table, g.seq_lens, W["uk8"], W["uk_s"], W["uv8"],
+                       W["uv_s"], g.scale, out, lse)
+        else:
+            m.run(g.q, g.cache, g.block_table, g.seq_lens, W["w_uk"], W["w_uv"], g.scale, out, lse)
     d = binding.dims_for(g.q, g.cache, g.block_table)
     m = binding.MlaDecode(d, dev)
     B, T, H = stats["B"], stats["T"], stats["H"]
@@ -300,10 +338,10 @@ def main():
 
     def step():
         m.plan(g.seq_lens)
-        m.absorb(g.q, g.w_uk)
+        absorb()
         m.attend(g.cache, g.block_table, g.seq_lens, g.scale, lse)
         m.combine(g.scale, lse)
-        m.up_project(g.w_uv, out)
+        up_project()
 
     def attend_only():
         m.attend(g.cache, g.block_table, g.seq_lens, g.scale, lse)
@@ -384,18 +422,19 @@ def main():
     per_step = elapsed / args.steps
 
     # ---- end to end through the same C ABI with host buffers
-    host = {k: getattr(inp_cpu, k).pin_memory() for k in
-            ("q", "cache", "block_table", "seq_lens", "w_uk", "w_uv")}
+    host = [(getattr(inp_cpu, k).pin_memory(), getattr(g, k)) for k in
+            ("q", "cache", "block_table", "seq_lens")]
+    host += [(h.pin_memory(), dv) for h, dv in wts.values()]
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(t.numel() * t.element_size() for t, _ in host)
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
 
     def e2e_step():
-        for k, t in host.items():
-            getattr(g, k).copy_(t, non_blocking=True)
+        for t, dv in host:
+            dv.copy_(t, non_blocking=True)
         m.plan(g.seq_lens)
-        m.run(g.q, g.cache, g.block_table, g.seq_lens, g.w_uk, g.w_uv, g.scale, out, lse)
+        run_all()
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 
@@ -416,9 +455,9 @@ def main():
 
     breakdown = None
     if args.breakdown:
-        stages = {"plan": lambda: m.plan(g.seq_lens), "absorb": lambda: m.absorb(g.q, g.w_uk),
+        stages = {"plan": lambda: m.plan(g.seq_lens), "absorb": absorb,
                   "attend": attend_only, "combine": lambda: m.combine(g.scale, lse),
-                  "up_project": lambda: m.up_project(g.w_uv, out)}
+                  "up_project": up_project}
         breakdown = {}
         for name, fn in stages.items():
             gr = torch.cuda.CUDAGraph()
@@ -463,6 +502,7 @@ def main():
                    "sum_seq_len": stats["sum_len"],
                    "seq_len": int(inp_cpu.seq_lens[0]) if len(set(inp_cpu.seq_lens.tolist())) == 1
                    else "varied", "page": 64, "parallelism": "replica x%d" % world,
+                   "weights": "fp8 e4m3, 128x128 block scales" if fp8 else "bf16",
                    "l2": "inputs larger than L2 (latent cache %.0f MB > 129 MB L2)" %
                          (stats["cache_bytes"] / 1e6)},
         "tflops": tflops, "tokens_per_s": world * stats["tokens"] / per_step,
@@ -482,7 +522,13 @@ def main():
         line["stage_us"] = breakdown
     if not args.no_cpu_baseline:
         import oracle
-        dt, nbytes, flops, tokens, text = time_oracle(inp_cpu, budget_s=15.0)
+        inp_or = inp_cpu
+        if fp8:  # the oracle decompresses the FP8 weights, then decodes
+            import copy
+            inp_or = copy.copy(inp_cpu)
+            inp_or.w_uk = oracle.dequant_fp8_weight(uk8, uk_s)
+            inp_or.w_uv = oracle.dequant_fp8_weight(uv8, uv_s)
+        dt, nbytes, flops, tokens, text = time_oracle(inp_or, budget_s=15.0)
         line["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s",
                                 "cores": oracle.threads(), "kind": "oracle", "sample": text,
                                 "seconds": dt, "tflops": flops / dt / 1e12}

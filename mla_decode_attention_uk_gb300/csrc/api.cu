@@ -108,17 +108,20 @@ EncodeTiledFn encoder() {
   return g_encode;
 }
 
-// 2-D bf16 tensor map: `rows` x `cols` (row stride `row_stride` elements),
-// box = box_cols x box_rows, 128-byte swizzle.
+// 2-D tensor map of bf16 (or, with elem_bytes = 1, byte) elements: `rows` x
+// `cols` (row stride `row_stride` elements), box = box_cols x box_rows,
+// 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t row_stride,
-              uint32_t box_cols, uint32_t box_rows, bool stream_hint) {
+              uint32_t box_cols, uint32_t box_rows, bool stream_hint, int elem_bytes = 2) {
   EncodeTiledFn enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {row_stride * 2};
+  cuuint64_t strides[1] = {row_stride * elem_bytes};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  CUresult r = enc(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    stream_hint ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
                                : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -285,10 +288,10 @@ static int absorb_impl(const mla_decode_dims* d, const void* q, const void* w_uk
   if (!make_map(&tm_q, q, BT, static_cast<uint64_t>(H) * kDq, static_cast<uint64_t>(H) * kDq,
                 kBoxCols, bmm_token_tile(BT), false))
     return MLA_DECODE_CUDA_ERROR;
-  if (w8)
-    tm_w = tm_q;  // not read: the kernel converts the FP8 weights itself
-  else if (!make_map(&tm_w, w_uk, static_cast<uint64_t>(H) * kNope, kLora, kLora, kBoxCols, 64,
-                     false))
+  // FP8 weights: 128-byte boxes of 128 m values x 64 k rows.
+  if (!(w8 ? make_map(&tm_w, w8, static_cast<uint64_t>(H) * kNope, kLora, kLora, 128, 64, false, 1)
+           : make_map(&tm_w, w_uk, static_cast<uint64_t>(H) * kNope, kLora, kLora, kBoxCols, 64,
+                      false)))
     return MLA_DECODE_CUDA_ERROR;
   return cuda_rc(launch_absorb(tm_w, tm_q, BT, H, static_cast<const __nv_bfloat16*>(q),
                                at<__nv_bfloat16>(ws, L.qlat), at<__nv_bfloat16>(ws, L.qlo),
@@ -313,10 +316,10 @@ static int up_project_impl(const mla_decode_dims* d, const void* w_uv, const uin
   if (!make_map(&tm_o, at<void>(ws, L.olat), BT, static_cast<uint64_t>(H) * kLora,
                 static_cast<uint64_t>(H) * kLora, kBoxCols, bmm_token_tile(BT), false))
     return MLA_DECODE_CUDA_ERROR;
-  if (w8)
-    tm_w = tm_o;  // not read: the kernel converts the FP8 weights itself
-  else if (!make_map(&tm_w, w_uv, static_cast<uint64_t>(H) * kLora, kVHead, kVHead, kBoxCols, 64,
-                     false))
+  if (!(w8 ? make_map(&tm_w, w8, static_cast<uint64_t>(H) * kLora, kVHead, kVHead, 128, 64, false,
+                      1)
+           : make_map(&tm_w, w_uv, static_cast<uint64_t>(H) * kLora, kVHead, kVHead, kBoxCols, 64,
+                      false)))
     return MLA_DECODE_CUDA_ERROR;
   return cuda_rc(launch_up_project(tm_w, tm_o, BT, H, static_cast<__nv_bfloat16*>(out),
                                    at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream),

@@ -21,10 +21,12 @@
 // FP8 weights (W8): the page says the absorbed form lacks an FP8 bmm, so the
 // matrices involved are decompressed to bf16 and the bmm runs in bf16.  Here
 // the decompression happens inside the bmm: W is stored as FP8 E4M3 with one
-// fp32 scale per 128 x 128 block, warps 2-3 load each stage's 64 x 128 FP8
-// tile, form W = bf16(fp32(w8) * scale) (fp32 product, round to nearest even)
-// and write it straight into the swizzled shared-memory layout the MMA reads,
-// while warp 0 brings the activation tile by TMA.
+// fp32 scale per 128 x 128 block.  Warps 2-3 keep a ring of raw 64 x 128 FP8
+// tiles filled by TMA (issued before the kernel waits for its predecessor:
+// the weights do not depend on it), form W = bf16(fp32(w8) * scale) (fp32
+// product, round to nearest even) and write it straight into the swizzled
+// shared-memory layout the MMA reads, while warp 0 brings the activation tile.
+// FP8 kernels run 192 threads: warps 2-5 convert.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -38,36 +40,73 @@ namespace mla {
 
 namespace {
 
-constexpr int kBmmThreads = 128;
+constexpr int kBmmThreads = 128;    // bf16 weights
+constexpr int kBmmThreadsW8 = 192;  // FP8 weights: four converter warps more
 constexpr int kABytes = 2 * kBoxBytes;  // 128 m x 64 k, two 64-wide m boxes
 
 enum class BmmMode { kAbsorb, kUpProject };
 
-// FP8 weights: E4M3 bytes [H, K, M] and fp32 scales [H, K/128, M/128].
+// FP8 weights: E4M3 bytes [H, K, M] (read through the W tensor map) and fp32
+// scales [H, K/128, M/128].
 struct Fp8Weights {
   const uint8_t* w;
   const float* scale;
   int M;
 };
 
-template <int NT, int STAGES>
+// Raw FP8 tiles kept in flight ahead of the converters: all of K = 128 for the
+// absorb step, half of K = 512 for the up-projection.
+__host__ __device__ constexpr int raw_tiles(BmmMode mode, bool w8) {
+  return !w8 ? 0 : (mode == BmmMode::kAbsorb ? 2 : 4);
+}
+constexpr int kRawBytes = 64 * 128;  // one FP8 tile: 64 k rows x 128 m bytes
+
+template <int NT, int STAGES, int RAWS>
 struct BmmSmem {
   static constexpr int kBBytes = NT * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kOutBytes = NT * 128 * 2;  // bf16 [NT tokens][128 m] staging tile
   static constexpr int kPipe = STAGES * kStageBytes;
-  static constexpr int kBody = kPipe > 2 * kOutBytes ? kPipe : 2 * kOutBytes;
+  static constexpr int kIn = kPipe + RAWS * kRawBytes;  // raw FP8 ring after the stages
+  static constexpr int kBody = kIn > 2 * kOutBytes ? kIn : 2 * kOutBytes;
   static constexpr int kTotal = kBody + 1024;  // + alignment slack
 };
 
+// Named barrier over `nthreads` threads that also returns the AND of `pred`
+// over them, so the threads leave a loop together.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 template <BmmMode MODE, int NT, int STAGES, bool W8>
-__global__ void __launch_bounds__(kBmmThreads)
+__global__ void __launch_bounds__(W8 ? kBmmThreadsW8 : kBmmThreads)
 bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
            int BT, int H, int K, int Kx, const __nv_bfloat16* __restrict__ q,
            __nv_bfloat16* __restrict__ out_hi, __nv_bfloat16* __restrict__ out_lo,
            int32_t* __restrict__ status, Fp8Weights w8) {
+  constexpr int RAWS = raw_tiles(MODE, W8);
+  constexpr int kRing = RAWS > 0 ? RAWS : 1;  // ring length as a divisor
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], done_bar;
+  // full_bar: the stage's TMA bytes; conv_bar: the converters' bf16 weight
+  // tile (W8); raw_bar: one raw FP8 tile's TMA bytes (W8).
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], done_bar,
+      conv_bar[W8 ? STAGES : 1], raw_bar[W8 ? RAWS : 1];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -83,21 +122,23 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   const int h = blockIdx.z;
   const int nk = K / 64;
   constexpr uint32_t kTmemCols = NT < 32 ? 32 : NT;
-  using S = BmmSmem<NT, STAGES>;
+  using S = BmmSmem<NT, STAGES, RAWS>;
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const sbase_ptr = smem_raw + (sbase - smem_u32(smem_raw));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      // FP8 weights: the TMA transaction and the converters' arrival.
-      mbar_init(smem_u32(&full_bar[s]), W8 ? 2 : 1);
+      mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
+      if constexpr (W8) mbar_init(smem_u32(&conv_bar[s]), 1);
     }
+    if constexpr (W8)
+      for (int r = 0; r < RAWS; ++r) mbar_init(smem_u32(&raw_bar[r]), 1);
     mbar_init(smem_u32(&done_bar), 1);
     abort_sh = 0;
     fence_mbar_init();
-    if (!W8) tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_x);
   }
   if (warp == 2) {
@@ -111,7 +152,7 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
 
   if (warp == 0) {
     if (elect_one()) {
-      int kc0 = 0;
+      int kc0 = 0, issued = 0;
       if constexpr (MODE == BmmMode::kUpProject) {
         kc0 = nk < STAGES ? nk : STAGES;
         for (int kc = 0; kc < kc0; ++kc) {
@@ -128,6 +169,7 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
           const uint32_t b = sbase + kc * S::kStageBytes + kABytes;
           tma_load_2d(b, &tm_x, h * Kx + kc * 64, tok0, smem_u32(&full_bar[kc]));
         }
+        issued = kc0;
       }
       for (int kc = kc0; kc < nk; ++kc) {
         const int s = kc % STAGES;
@@ -143,28 +185,55 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
           tma_load_2d(a + kBoxBytes, &tm_w, m0 + 64, h * K + kc * 64, fb);
         }
         tma_load_2d(b, &tm_x, h * Kx + kc * 64, tok0, fb);
+        issued = kc + 1;
+      }
+      // Copies still in flight (only after a timeout) must land before the
+      // CTA exits: wait for the last load of each stage.
+      for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
+        mbar_wait_drain(smem_u32(&full_bar[j % STAGES]), (j / STAGES) & 1, status);
+    }
+  } else if (W8 && warp >= 2 && warp < 6) {
+    // FP8 weight converters: thread ct (0..127) owns m columns 64 half ..
+    // 64 half + 63 of k row kr of each stage's 64 x 128 weight tile.  Raw
+    // tiles arrive by TMA with 128B swizzle (16-byte chunk c of row r at chunk
+    // c ^ (r & 7)).  The bf16 tile is written in the layout TMA gives a bf16
+    // W: two 64-column m boxes (one per half), 128-byte rows, same swizzle.
+    // The two halves of a row visit their chunks in opposite order (jj =
+    // j ^ 2 half), so a quarter-warp's 16-byte reads and writes fall on eight
+    // distinct chunk positions: no bank conflicts.
+    const int ct = threadIdx.x - 64;
+    const int kr = ct >> 1, half = ct & 1;
+    const uint32_t raw0 = sbase + S::kPipe;
+    int raw_issued = 0;
+    if (ct == 0) {
+      for (; raw_issued < RAWS && raw_issued < nk; ++raw_issued) {
+        const uint32_t rb = smem_u32(&raw_bar[raw_issued]);
+        mbar_expect_tx(rb, kRawBytes);
+        tma_load_2d(raw0 + raw_issued * kRawBytes, &tm_w, m0, h * K + raw_issued * 64, rb);
       }
     }
-  } else if (W8 && warp >= 2) {
-    // FP8 weight converters: thread kr (0..63) owns k row kr of each stage's
-    // 64 x 128 weight tile.  The tile's bf16 layout is the one TMA would have
-    // produced: two 64-column m boxes, 128-byte rows, 16-byte chunks swizzled
-    // by the row index (128B swizzle).
-    const int kr = threadIdx.x - 64;
-    for (int kc = 0; kc < nk; ++kc) {
-      const int s = kc % STAGES;
-      if (kc >= STAGES &&
-          !mbar_wait(smem_u32(&empty_bar[s]), ((kc / STAGES) - 1) & 1, &abort_sh, status))
-        break;
-      const uint32_t a = sbase + s * S::kStageBytes;
-      const size_t krow = static_cast<size_t>(h) * K + kc * 64 + kr;
-      const uint4* src = reinterpret_cast<const uint4*>(w8.w + krow * w8.M + m0);
-      const float sc =
-          __ldg(w8.scale + (static_cast<size_t>(h) * (K / 128) + (kc * 64) / 128) * (w8.M / 128) +
-                m0 / 128);
+    // The scales of this m block: one per 128 k rows (K / 128 <= 4).
+    const float* scp = w8.scale + static_cast<size_t>(h) * (K / 128) * (w8.M / 128) + m0 / 128;
+    float scl[4];
 #pragma unroll
-      for (int qd = 0; qd < 8; ++qd) {  // 16 weights (m) per 16-byte load
-        const uint4 raw = __ldg(src + qd);
+    for (int i = 0; i < 4; ++i) scl[i] = i < K / 128 ? __ldg(scp + i * (w8.M / 128)) : 0.0f;
+    int kc = 0;
+    for (; kc < nk; ++kc) {
+      const int s = kc % STAGES, r = kc % kRing;
+      bool ok = true;
+      if (kc >= STAGES)
+        ok = mbar_wait(smem_u32(&empty_bar[s]), ((kc / STAGES) - 1) & 1, &abort_sh, status);
+      if (ok) ok = mbar_wait(smem_u32(&raw_bar[r]), (kc / kRing) & 1, &abort_sh, status);
+      if (!named_bar_and(1, 128, ok)) break;
+      const uint32_t rrow = raw0 + r * kRawBytes + kr * 128;
+      const uint32_t arow = sbase + s * S::kStageBytes + half * kBoxBytes + kr * 128;
+      const int kb = kc >> 1;  // 128-row scale block of this 64-row tile
+      const float sc = kb == 0 ? scl[0] : kb == 1 ? scl[1] : kb == 2 ? scl[2] : scl[3];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // 16 weights (m) per 16-byte chunk
+        const int jj = j ^ (half << 1);
+        const int qd = half * 4 + jj;
+        const uint4 raw = ld_shared_v4(rrow + ((qd ^ (kr & 7)) << 4));
         const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
         uint32_t ow[8];
 #pragma unroll
@@ -175,21 +244,36 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
           const __nv_bfloat162 bv = __floats2bfloat162_rn(f.x * sc, f.y * sc);
           ow[e] = *reinterpret_cast<const uint32_t*>(&bv);
         }
-        const int box = qd >> 2, c0 = 2 * (qd & 3);
-        const uint32_t row = a + box * kBoxBytes + kr * 128;
-        st_shared_v4(row + ((c0 ^ (kr & 7)) << 4), ow[0], ow[1], ow[2], ow[3]);
-        st_shared_v4(row + (((c0 + 1) ^ (kr & 7)) << 4), ow[4], ow[5], ow[6], ow[7]);
+        const int c0 = 2 * jj;
+        st_shared_v4(arow + ((c0 ^ (kr & 7)) << 4), ow[0], ow[1], ow[2], ow[3]);
+        st_shared_v4(arow + (((c0 + 1) ^ (kr & 7)) << 4), ow[4], ow[5], ow[6], ow[7]);
       }
+      // The bf16 tile goes to the tensor core and raw tile r back to TMA:
+      // order these threads' shared-memory accesses before both.
       fence_proxy_async_smem();
-      named_bar_sync(1, 64);
-      if (kr == 0) mbar_arrive(smem_u32(&full_bar[s]));
+      named_bar_sync(1, 128);
+      if (ct == 0) {
+        mbar_arrive(smem_u32(&conv_bar[s]));
+        if (raw_issued < nk) {
+          const uint32_t rb = smem_u32(&raw_bar[r]);
+          mbar_expect_tx(rb, kRawBytes);
+          tma_load_2d(raw0 + r * kRawBytes, &tm_w, m0, h * K + raw_issued * 64, rb);
+          ++raw_issued;
+        }
+      }
     }
+    // After a timeout, let the raw tiles still in flight land before exiting.
+    if (ct == 0)
+      for (int j = kc; j < raw_issued; ++j)
+        mbar_wait_drain(smem_u32(&raw_bar[j % kRing]), (j / kRing) & 1, status);
   } else if (warp == 1) {
     if (elect_one()) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, NT, /*a_mn=*/true, /*b_mn=*/false);
       for (int kc = 0; kc < nk; ++kc) {
         const int s = kc % STAGES;
         if (!mbar_wait(smem_u32(&full_bar[s]), (kc / STAGES) & 1, &abort_sh, status)) break;
+        if constexpr (W8)
+          if (!mbar_wait(smem_u32(&conv_bar[s]), (kc / STAGES) & 1, &abort_sh, status)) break;
         tc_fence_after();
         const uint32_t a = sbase + s * S::kStageBytes;
         const uint32_t b = a + kABytes;
@@ -206,17 +290,18 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   }
   __syncwarp();
 
-  // Epilogue.  Thread (warp w, lane i) owns feature m0 + 32 w + i: it moves its
-  // accumulator column (one value per token) into a bf16 [token][128 m] tile in
-  // the now idle pipeline smem, then all threads copy whole 256-byte token rows
-  // to global memory with 16-byte stores.
+  // Epilogue.  Thread (warp w < 4, lane i) owns feature m0 + 32 w + i: it
+  // moves its accumulator column (one value per token) into a bf16
+  // [token][128 m] tile in the now idle pipeline smem, then all threads copy
+  // whole 256-byte token rows to global memory with 16-byte stores.
+  constexpr int kThreads = W8 ? kBmmThreadsW8 : kBmmThreads;
   const bool have = mbar_wait(smem_u32(&done_bar), 0, &abort_sh, status);
   tc_fence_after();
   const int ml = warp * 32 + lane;
   __nv_bfloat16* const tile_hi = reinterpret_cast<__nv_bfloat16*>(sbase_ptr);
   __nv_bfloat16* const tile_lo = tile_hi + NT * 128;
   const bool go = have && !abort_sh;
-  if (go) {
+  if (go && warp < 4) {  // a warp reaches TMEM lanes 32 (warp % 4) .. + 31
 #pragma unroll 1
     for (int c0 = 0; c0 < NT; c0 += 16) {
       uint32_t r[16];
@@ -235,8 +320,8 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   __syncthreads();
   if (go) {
     const int ntok = min(NT, BT - tok0);
-    // 16 chunks of 16 B per token row; 128 threads cover 8 rows per pass.
-    for (int i = threadIdx.x; i < ntok * 16; i += kBmmThreads) {
+    // 16 chunks of 16 B per token row.
+    for (int i = threadIdx.x; i < ntok * 16; i += kThreads) {
       const int tl = i >> 4, ch = i & 15;
       const size_t row = static_cast<size_t>(tok0 + tl) * H + h;
       const uint4 vh = *reinterpret_cast<const uint4*>(tile_hi + tl * 128 + ch * 8);
@@ -251,7 +336,7 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
     if constexpr (MODE == BmmMode::kAbsorb) {
       // q_pe passes through unchanged into columns 512..575 (8 chunks of 16 B).
       if (blockIdx.y == 0) {
-        for (int i = threadIdx.x; i < ntok * 8; i += kBmmThreads) {
+        for (int i = threadIdx.x; i < ntok * 8; i += kThreads) {
           const int tl = i >> 3, ch = i & 7;
           const size_t row = static_cast<size_t>(tok0 + tl) * H + h;
           *reinterpret_cast<uint4*>(out_hi + row * kDqk + kLora + ch * 8) =
@@ -278,11 +363,12 @@ cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, 
   // stages, three CTAs per SM); four for the up-projection's smaller tiles.
   constexpr int STAGES = (MODE == BmmMode::kAbsorb || NT == 128) ? 2 : 4;
   auto kern = w8.w ? bmm_kernel<MODE, NT, STAGES, true> : bmm_kernel<MODE, NT, STAGES, false>;
-  const int smem = BmmSmem<NT, STAGES>::kTotal;
+  const int smem = w8.w ? BmmSmem<NT, STAGES, raw_tiles(MODE, true)>::kTotal
+                        : BmmSmem<NT, STAGES, 0>::kTotal;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((BT + NT - 1) / NT, Mtot / 128, H);
-  e = launch_pdl(kern, grid, dim3(kBmmThreads), smem, st, tw, tx, BT, H, K, Kx, q, hi, lo,
+  e = launch_pdl(kern, grid, dim3(w8.w ? kBmmThreadsW8 : kBmmThreads), smem, st, tw, tx, BT, H, K, Kx, q, hi, lo,
                  status, w8);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
