@@ -86,12 +86,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // then leaves its loop so the CTA can tear down cleanly.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           int* status) {
+  // The polling loops stay rolled: each inlined copy of a wait would
+  // otherwise add hundreds of instructions, and the kernels' warp roles run
+  // different code at the same time (measured: unrolled copies cost 1-3 %).
+#pragma unroll 1
   for (int i = 0; i < 256; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     // Poll the barrier many times per timer read and abort check, so a
     // completed phase is seen within a few polls.
+#pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
