@@ -37,8 +37,11 @@
  * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *   All work is enqueued on it; calls do not synchronise the host, except
  *   mla_decode_check.
- * - Return value: an mla_decode_status.  Codes 1..4 are detected on the host
- *   before anything is enqueued (nothing runs).  Codes 5..6 are detected by the
+ * - Return value: an mla_decode_status.  Codes 1..3 are detected on the host
+ *   before anything is enqueued (nothing runs); the whole-run calls check
+ *   every argument of all their steps first.  Code 4 reports a failed CUDA
+ *   call (tensor-map encoding, launch); for a whole-run call the steps before
+ *   the failing one may already be enqueued.  Codes 5..6 are detected by the
  *   kernels, written to the workspace status word and reported by
  *   mla_decode_check; the offending unit of work is skipped or computed on a
  *   substitute page, never trapped.

@@ -397,11 +397,35 @@ int mla_decode_up_project_fp8w(const mla_decode_dims* d, const uint8_t* w_uv_fp8
   return up_project_impl(d, nullptr, w_uv_fp8, w_uv_scale, out, ws, ws_bytes, stream);
 }
 
+// Every argument of a whole run, checked before its first launch so that a
+// host-detected error leaves nothing enqueued.  w_uk / w_uv are the bf16
+// weights, or with fp8 the E4M3 codes, whose block scales must then be given.
+static int check_run(const mla_decode_dims* d, const void* q, const void* kv_cache,
+                     const int32_t* block_table, const int32_t* seq_lens, const void* w_uk,
+                     const void* w_uv, bool fp8, const float* uk_scale, const float* uv_scale,
+                     const void* out, const float* lse, const void* ws, size_t ws_bytes) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  auto aligned4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!q || !kv_cache || !block_table || !seq_lens || !w_uk || !w_uv || !out || !lse || !ws ||
+      !aligned16(q) || !aligned16(kv_cache) || !aligned16(w_uk) || !aligned16(w_uv) ||
+      !aligned16(out) || !aligned16(ws) || !aligned4(block_table) || !aligned4(seq_lens) ||
+      !aligned4(lse))
+    return MLA_DECODE_INVALID_ARG;
+  if (fp8 && (!uk_scale || !uv_scale || !aligned4(uk_scale) || !aligned4(uv_scale)))
+    return MLA_DECODE_INVALID_ARG;
+  WsLayout L;
+  return layout_for(d, ws_bytes, &L);
+}
+
 int mla_decode_run(const mla_decode_dims* d, const void* q, const void* kv_cache,
                    const int32_t* block_table, const int32_t* seq_lens, const void* w_uk,
                    const void* w_uv, float scale, void* out, float* lse, void* ws, size_t ws_bytes,
                    void* stream) {
-  int rc = mla_decode_absorb(d, q, w_uk, ws, ws_bytes, stream);
+  int rc = check_run(d, q, kv_cache, block_table, seq_lens, w_uk, w_uv, false, nullptr, nullptr,
+                     out, lse, ws, ws_bytes);
+  if (rc) return rc;
+  rc = mla_decode_absorb(d, q, w_uk, ws, ws_bytes, stream);
   if (rc) return rc;
   rc = mla_decode_attend(d, kv_cache, block_table, seq_lens, scale, lse, ws, ws_bytes, stream);
   if (rc) return rc;
@@ -415,7 +439,10 @@ int mla_decode_run_fp8w(const mla_decode_dims* d, const void* q, const void* kv_
                         const uint8_t* w_uk_fp8, const float* w_uk_scale,
                         const uint8_t* w_uv_fp8, const float* w_uv_scale, float scale, void* out,
                         float* lse, void* ws, size_t ws_bytes, void* stream) {
-  int rc = mla_decode_absorb_fp8w(d, q, w_uk_fp8, w_uk_scale, ws, ws_bytes, stream);
+  int rc = check_run(d, q, kv_cache, block_table, seq_lens, w_uk_fp8, w_uv_fp8, true, w_uk_scale,
+                     w_uv_scale, out, lse, ws, ws_bytes);
+  if (rc) return rc;
+  rc = mla_decode_absorb_fp8w(d, q, w_uk_fp8, w_uk_scale, ws, ws_bytes, stream);
   if (rc) return rc;
   rc = mla_decode_attend(d, kv_cache, block_table, seq_lens, scale, lse, ws, ws_bytes, stream);
   if (rc) return rc;

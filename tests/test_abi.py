@@ -107,3 +107,42 @@ def test_workspace_too_small_rejected_before_launch():
     ok = ctypes.c_void_p(4096)
     assert L.mla_decode_absorb(ctypes.byref(d), ok, ok, ok, 64, None) == 3
     assert L.mla_decode_combine(ctypes.byref(d), ctypes.c_float(0.07), ok, ok, 64, None) == 3
+
+
+def test_run_checks_every_argument_before_the_first_launch():
+    # A bad argument of a late step (the up-projection's weight, an output)
+    # must be reported before the absorb step is enqueued.  Without a GPU an
+    # enqueue attempt fails with CUDA_ERROR (4), so INVALID_ARG (1) shows that
+    # the check came first.
+    L = binding.lib()
+    d = good_dims()
+    ok, bad = ctypes.c_void_p(4096), ctypes.c_void_p(4096 + 2)
+    sc = ctypes.c_float(0.07)
+    assert L.mla_decode_run(ctypes.byref(d), ok, ok, ok, ok, ok, None, sc, ok, ok, ok,
+                            1 << 30, None) == 1
+    assert L.mla_decode_run(ctypes.byref(d), ok, ok, ok, ok, ok, bad, sc, ok, ok, ok,
+                            1 << 30, None) == 1
+    assert L.mla_decode_run(ctypes.byref(d), ok, ok, ok, ok, ok, ok, sc, bad, ok, ok,
+                            1 << 30, None) == 1
+    assert L.mla_decode_run(ctypes.byref(d), ok, ok, ok, ctypes.c_void_p(4097), ok, ok, sc, ok,
+                            ok, ok, 1 << 30, None) == 1
+    assert L.mla_decode_run(ctypes.byref(d), ok, ok, ok, ok, ok, ok, sc, ok, ok, ok, 64,
+                            None) == 3
+    # FP8 weights: codes and both block-scale arrays.
+    args = [ok, ok, ok, ok, ok, ok, ok, ok, sc, ok, ok, ok]
+    for i, v in ((6, None), (7, None), (7, ctypes.c_void_p(4097)), (6, bad)):
+        a = list(args)
+        a[i] = v
+        assert L.mla_decode_run_fp8w(ctypes.byref(d), *a, 1 << 30, None) == 1, i
+
+
+def test_fp8_step_calls_check_their_scales():
+    L = binding.lib()
+    d = good_dims()
+    ok = ctypes.c_void_p(4096)
+    assert L.mla_decode_absorb_fp8w(ctypes.byref(d), ok, ok, None, ok, 1 << 30, None) == 1
+    assert L.mla_decode_absorb_fp8w(ctypes.byref(d), ok, None, ok, ok, 1 << 30, None) == 1
+    assert L.mla_decode_up_project_fp8w(ctypes.byref(d), ok, ctypes.c_void_p(4098), ok, ok,
+                                        1 << 30, None) == 1
+    assert L.mla_decode_up_project_fp8w(ctypes.byref(d), ok, ok, ok, ok, 64, None) == 3
+
