@@ -289,12 +289,42 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
     }
   }
   __syncwarp();
+  constexpr int kThreads = W8 ? kBmmThreadsW8 : kBmmThreads;
+
+  if constexpr (MODE == BmmMode::kAbsorb) {
+    // q_pe passes through unchanged into columns 512..575 of q_lat (8 chunks
+    // of 16 B per token).  The helper warps (2 and up: idle, or done
+    // converting) copy it while the MMAs run, all loads before the stores,
+    // so the copy costs one memory round trip instead of one per chunk.
+    if (blockIdx.y == 0 && warp >= 2) {
+      constexpr int kHelpers = kThreads - 64;
+      constexpr int kIters = (NT * 8 + kHelpers - 1) / kHelpers;
+      const int nchunks = min(NT, BT - tok0) * 8;
+      const int t0 = threadIdx.x - 64;
+      uint4 v[kIters];
+#pragma unroll
+      for (int it = 0; it < kIters; ++it) {
+        const int i = t0 + it * kHelpers;
+        if (i < nchunks) {
+          const size_t row = static_cast<size_t>(tok0 + (i >> 3)) * H + h;
+          v[it] = *reinterpret_cast<const uint4*>(q + row * kDq + kNope + (i & 7) * 8);
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < kIters; ++it) {
+        const int i = t0 + it * kHelpers;
+        if (i < nchunks) {
+          const size_t row = static_cast<size_t>(tok0 + (i >> 3)) * H + h;
+          *reinterpret_cast<uint4*>(out_hi + row * kDqk + kLora + (i & 7) * 8) = v[it];
+        }
+      }
+    }
+  }
 
   // Epilogue.  Thread (warp w < 4, lane i) owns feature m0 + 32 w + i: it
   // moves its accumulator column (one value per token) into a bf16
   // [token][128 m] tile in the now idle pipeline smem, then all threads copy
   // whole 256-byte token rows to global memory with 16-byte stores.
-  constexpr int kThreads = W8 ? kBmmThreadsW8 : kBmmThreads;
   const bool have = mbar_wait(smem_u32(&done_bar), 0, &abort_sh, status);
   tc_fence_after();
   const int ml = warp * 32 + lane;
@@ -331,17 +361,6 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
         *reinterpret_cast<uint4*>(out_lo + row * kLora + m0 + ch * 8) = vl;
       } else {
         *reinterpret_cast<uint4*>(out_hi + row * kVHead + m0 + ch * 8) = vh;
-      }
-    }
-    if constexpr (MODE == BmmMode::kAbsorb) {
-      // q_pe passes through unchanged into columns 512..575 (8 chunks of 16 B).
-      if (blockIdx.y == 0) {
-        for (int i = threadIdx.x; i < ntok * 8; i += kThreads) {
-          const int tl = i >> 3, ch = i & 7;
-          const size_t row = static_cast<size_t>(tok0 + tl) * H + h;
-          *reinterpret_cast<uint4*>(out_hi + row * kDqk + kLora + ch * 8) =
-              *reinterpret_cast<const uint4*>(q + row * kDq + kNope + ch * 8);
-        }
       }
     }
   }

@@ -227,13 +227,16 @@ def test_full_size_workloads_sampled(name):
     assert_parity(compare(inp, out, lse, rows=rows), name)
 
 
-@pytest.mark.parametrize("B,T,H", [(3, 1, 16), (20, 1, 64), (40, 2, 128)])
+@pytest.mark.parametrize("B,T,H", [(3, 1, 16), (20, 1, 64), (64, 1, 16), (40, 2, 128),
+                                   (100, 2, 16), (72, 8, 32)])
 def test_fp8_weights_equal_bf16_run_on_decompressed_weights(B, T, H):
-    # 16-, 32- and 128-token bmm tiles.  The kernels decompress each FP8 weight
-    # tile to bf16 as they load it; the result must equal, bit for bit, the bf16
-    # path given the weights the oracle decompresses, and match the oracle.
-    g = torch.Generator().manual_seed(60 + H)
-    lens = torch.randint(T, 900, (B,), generator=g).tolist()
+    # 16-, 32-, 64- and 128-token bmm tiles, up to five 128-token tiles per
+    # head with a ragged last one (576 tokens).  The kernels decompress each
+    # FP8 weight tile to bf16 as they load it; the result must equal, bit for
+    # bit, the bf16 path given the weights the oracle decompresses, and match
+    # the oracle.
+    g = torch.Generator().manual_seed(60 + H + B)
+    lens = torch.randint(T, 900 if B * T <= 256 else 300, (B,), generator=g).tolist()
     inp = make_inputs(B, lens, T, H, seed=61 + H)
     uk8, uk_s = quantize_fp8_blockwise(inp.w_uk)
     uv8, uv_s = quantize_fp8_blockwise(inp.w_uv)
@@ -253,4 +256,28 @@ def test_fp8_weights_equal_bf16_run_on_decompressed_weights(B, T, H):
     assert m.check() == 0
     assert torch.equal(o8, ob) and torch.equal(l8, lb)
     assert_parity(compare(inp, o8.cpu(), l8.cpu()), "fp8 weights B=%d T=%d H=%d" % (B, T, H))
+
+
+@pytest.mark.parametrize("name", ["tp_shard", "mixed_spec"])
+def test_full_size_fp8_weights_sampled(name):
+    # The bench's FP8 configuration at full size: 64-token tiles (tp_shard)
+    # and four 128-token tiles per head (mixed_spec), on sampled rows.
+    inp = workload_inputs(name)
+    uk8, uk_s = quantize_fp8_blockwise(inp.w_uk)
+    uv8, uv_s = quantize_fp8_blockwise(inp.w_uv)
+    inp.w_uk = oracle.dequant_fp8_weight(uk8, uk_s)
+    inp.w_uv = oracle.dequant_fp8_weight(uv8, uv_s)
+    dev = torch.device("cuda")
+    gd = inp.to(dev)
+    B, T, H = inp.q.shape[:3]
+    d = binding.dims_for(gd.q, gd.cache, gd.block_table)
+    m = binding.MlaDecode(d, dev)
+    out = torch.empty(B, T, H, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, T, H, dtype=torch.float32, device=dev)
+    m.plan(gd.seq_lens)
+    m.run_fp8w(gd.q, gd.cache, gd.block_table, gd.seq_lens, uk8.to(dev), uk_s.to(dev),
+               uv8.to(dev), uv_s.to(dev), gd.scale, out, lse)
+    assert m.check() == 0
+    rows = sample_rows(inp, 96, seed=2)
+    assert_parity(compare(inp, out.cpu(), lse.cpu(), rows=rows), "fp8 weights " + name)
 
