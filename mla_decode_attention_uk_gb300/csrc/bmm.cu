@@ -332,13 +332,18 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   __nv_bfloat16* const tile_lo = tile_hi + NT * 128;
   const bool go = have && !abort_sh;
   if (go && warp < 4) {  // a warp reaches TMEM lanes 32 (warp % 4) .. + 31
+    constexpr int kCols = NT >= 32 ? 32 : 16;  // tokens per TMEM load
 #pragma unroll 1
-    for (int c0 = 0; c0 < NT; c0 += 16) {
-      uint32_t r[16];
-      tmem_ld_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, r);
+    for (int c0 = 0; c0 < NT; c0 += kCols) {
+      uint32_t r[kCols];
+      const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0;
+      if constexpr (kCols == 32)
+        tmem_ld_x32(ta, r);
+      else
+        tmem_ld_x16(ta, r);
       tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < kCols; ++j) {
         const float v = __uint_as_float(r[j]);
         const __nv_bfloat16 hv = __float2bfloat16_rn(v);
         tile_hi[(c0 + j) * 128 + ml] = hv;

@@ -53,6 +53,8 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
     const uint4* l4 = reinterpret_cast<const uint4*>(qlo + row * kLora) + lane * 2;
     const uint4 lv0 = l4[0], lv1 = l4[1];
     griddep_wait();
+    // The row's lse goes out with the o_lat loads: one round trip, not two.
+    const float lse_in = lane == 0 ? lse_out[row] : 0.0f;
     float corr = 0.0f;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
@@ -68,7 +70,7 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) corr += __shfl_xor_sync(0xffffffffu, corr, o);
-    if (lane == 0) lse_out[row] += scale * corr;
+    if (lane == 0) lse_out[row] = lse_in + scale * corr;
     return;
   }
   const int slot0 = seq_slot[b];
