@@ -472,6 +472,9 @@ def main():
             b1.record(stream)
             torch.cuda.synchronize()
             breakdown[name] = b0.elapsed_time(b1) / 200 * 1e3
+        st = m.check()
+        if st != 0:
+            raise SystemExit("device status %d in the per-stage timing" % st)
 
     if rank != 0:
         dist.destroy_process_group()

@@ -38,7 +38,7 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
 cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, const void* ws,
                            const PlanHeader* header, const __nv_bfloat16* qlo,
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
-                           cudaStream_t st);
+                           bool many_splits, cudaStream_t st);
 }  // namespace mla
 
 namespace {
@@ -378,10 +378,17 @@ int mla_decode_combine(const mla_decode_dims* d, float scale, float* lse, void* 
   WsLayout L;
   rc = layout_for(d, ws_bytes, &L);
   if (rc) return rc;
+  // With at least as many work ranges as sequences, sequences are typically
+  // cut into several splits; with fewer, most rows are unsplit.  (Only the
+  // speed depends on this guess: both combine variants compute the same.)
+  int ranges = 0;
+  rc = default_ranges(d, &ranges);
+  if (rc) return rc;
   return cuda_rc(launch_combine(at<int32_t>(ws, L.seq_nsplit), at<int32_t>(ws, L.seq_slot), ws,
                                 at<PlanHeader>(ws, L.header), at<__nv_bfloat16>(ws, L.qlo),
                                 at<__nv_bfloat16>(ws, L.olat), lse, d->batch, d->q_len,
-                                d->num_heads, scale, static_cast<cudaStream_t>(stream)));
+                                d->num_heads, scale, ranges >= d->batch,
+                                static_cast<cudaStream_t>(stream)));
 }
 
 int mla_decode_up_project(const mla_decode_dims* d, const void* w_uv, void* out, void* ws,

@@ -14,7 +14,11 @@
 // scale * (q_lo . o) restores the scores of the full-precision query up to
 // second order in q_lo (|q_lo| <= 2^-9 |q_lat|).
 // One warp per query row; each lane owns 16 of the 512 latent columns and
-// moves them with 16-byte vector loads.
+// moves them with 16-byte vector loads.  Two instantiations differ in how far
+// the loop over a row's splits is unrolled: by 4 when sequences are cut into
+// many splits (more loads in flight per warp), or not at all when most rows
+// are unsplit (64 registers instead of 70, so four CTAs fit on an SM instead
+// of three).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -28,6 +32,7 @@ namespace {
 constexpr int kCombThreads = 256;
 constexpr int kRowsPerCta = kCombThreads / 32;
 
+template <int kUnroll>
 __global__ void __launch_bounds__(kCombThreads)
 combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict__ seq_slot,
                const uint8_t* __restrict__ ws, const PlanHeader* __restrict__ header, int B,
@@ -111,7 +116,7 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
                                    : -INFINITY;
     const float wl = (l == -INFINITY) ? 0.0f : __expf(l - lse);  // weight of split s0 + lane
     const int n = min(32, ns - s0);
-#pragma unroll 4
+#pragma unroll kUnroll
     for (int i = 0; i < n; ++i) {
       const float w = __shfl_sync(0xffffffffu, wl, i);
       const float4* src = reinterpret_cast<const float4*>(
@@ -152,11 +157,12 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
 cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, const void* ws,
                            const PlanHeader* header, const __nv_bfloat16* qlo,
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
-                           cudaStream_t st) {
+                           bool many_splits, cudaStream_t st) {
   dim3 grid((T * H + kRowsPerCta - 1) / kRowsPerCta, B);
-  cudaError_t e = launch_pdl(combine_kernel, grid, dim3(kCombThreads), 0, st, seq_nsplit,
-                             seq_slot, static_cast<const uint8_t*>(ws), header, B, T, H, qlo, olat,
-                             lse, scale);
+  auto kern = many_splits ? combine_kernel<4> : combine_kernel<1>;
+  cudaError_t e = launch_pdl(kern, grid, dim3(kCombThreads), 0, st, seq_nsplit, seq_slot,
+                             static_cast<const uint8_t*>(ws), header, B, T, H, qlo, olat, lse,
+                             scale);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
