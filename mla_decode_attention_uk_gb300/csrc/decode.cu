@@ -65,10 +65,7 @@ constexpr uint64_t kLoadOrder = 0x876325410ull;    // 0, 1, 4, 5, 2, 3, 6, 7, 8
 constexpr uint64_t kQkOrder0 = 0x32410ull;         // 0, 1, 4, 2, 3
 constexpr uint64_t kQkOrder1 = 0x8765ull;          // 5, 6, 7, 8
 __host__ __device__ constexpr int free_group(int box) { return box == kRopeBox ? 4 : box >> 1; }
-#ifndef MLA_PREFETCH_PAGES
-#define MLA_PREFETCH_PAGES 2
-#endif
-constexpr int kPrefetchPages = MLA_PREFETCH_PAGES;  // L2 prefetch distance, in pages
+constexpr int kPrefetchPages = 2;                  // L2 prefetch distance, in pages
 constexpr int kDynSmemMax = 232448 - 2048;         // opt-in limit minus static smem budget
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;                   // O^T blocks at 256 + 64 m
