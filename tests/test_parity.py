@@ -78,6 +78,29 @@ def test_split_counts_long_drafts(num_ranges):
     assert_parity(compare(inp, out, lse), "T=8 R=%d" % num_ranges)
 
 
+@pytest.mark.parametrize("T", [1, 2])
+def test_many_short_sequences_plan_in_global_memory(T):
+    # More sequences than the planner keeps in shared memory (4096): its cost
+    # prefix and per-range searches run from global memory.  Lengths up to
+    # 130 tokens, page boundaries included; 16 heads.
+    g = torch.Generator().manual_seed(71 + T)
+    B = 5000
+    lens = torch.randint(T, 131, (B,), generator=g).tolist()
+    lens[:6] = [T, 63, 64, 65, 128, 130]
+    inp = make_inputs(B, lens, T, 16, seed=72 + T)
+    out, lse, _ = run_gpu(inp)
+    assert_parity(compare(inp, out, lse), "B=%d T=%d" % (B, T))
+
+
+def test_one_very_long_sequence_split_over_every_range():
+    # One sequence of 131072 tokens (2048 pages): every work range takes a
+    # piece of it, so the combine merges more than 32 splits per row.
+    inp = make_inputs(1, [131072], 1, 16, seed=73)
+    out, lse, m = run_gpu(inp)
+    assert m.plan_header()[0] > 32
+    assert_parity(compare(inp, out, lse), "L=131072")
+
+
 def test_split_counts_h128():
     lens = [900, 2000, 70]
     inp = make_inputs(len(lens), lens, 1, 128, seed=8)
