@@ -17,7 +17,7 @@ cudaError_t launch_plan(const int32_t* seq_lens, int B, int T, int max_pages, in
                         int32_t* status, PlanHeader* header, int32_t* range_b, int32_t* range_p,
                         int32_t* seq_first, int32_t* seq_nsplit, int32_t* seq_slot,
                         int32_t* seq_len_eff, int32_t* prefix, cudaStream_t stream);
-int bmm_token_tile(int BT);
+int bmm_token_tile(int BT, bool absorb);
 cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q, int BT, int H,
                           const __nv_bfloat16* q, __nv_bfloat16* qlat, __nv_bfloat16* qlo,
                           int32_t* status, cudaStream_t st, const uint8_t* wuk8,
@@ -286,7 +286,7 @@ static int absorb_impl(const mla_decode_dims* d, const void* q, const void* w_uk
   const int BT = d->batch * d->q_len, H = d->num_heads;
   CUtensorMap tm_q, tm_w;
   if (!make_map(&tm_q, q, BT, static_cast<uint64_t>(H) * kDq, static_cast<uint64_t>(H) * kDq,
-                kBoxCols, bmm_token_tile(BT), false))
+                kBoxCols, bmm_token_tile(BT, true), false))
     return MLA_DECODE_CUDA_ERROR;
   // FP8 weights: 128-byte boxes of 128 m values x 64 k rows.
   if (!(w8 ? make_map(&tm_w, w8, static_cast<uint64_t>(H) * kNope, kLora, kLora, 128, 64, false, 1)
@@ -314,7 +314,7 @@ static int up_project_impl(const mla_decode_dims* d, const void* w_uv, const uin
   const int BT = d->batch * d->q_len, H = d->num_heads;
   CUtensorMap tm_o, tm_w;
   if (!make_map(&tm_o, at<void>(ws, L.olat), BT, static_cast<uint64_t>(H) * kLora,
-                static_cast<uint64_t>(H) * kLora, kBoxCols, bmm_token_tile(BT), false))
+                static_cast<uint64_t>(H) * kLora, kBoxCols, bmm_token_tile(BT, false), false))
     return MLA_DECODE_CUDA_ERROR;
   if (!(w8 ? make_map(&tm_w, w8, static_cast<uint64_t>(H) * kLora, kVHead, kVHead, 128, 64, false,
                       1)

@@ -401,10 +401,15 @@ cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, 
 }  // namespace
 
 // Token tile used for a given token count (also the TMA box height of X).
-int bmm_token_tile(int BT) {
+// The absorb step keeps 64-token tiles up to 128 tokens: one 128-token tile
+// per head and m block would give 4 H CTAs at three per SM, just over one
+// wave for 128 heads, where 64-token tiles run four per SM with half the
+// epilogue each (measured: 14.3 -> 12.3 us for 128 tokens x 128 heads).  For
+// more tokens the larger tiles win (fewer weight re-reads).
+int bmm_token_tile(int BT, bool absorb) {
   if (BT <= 16) return 16;
   if (BT <= 32) return 32;
-  if (BT <= 64) return 64;
+  if (BT <= 64 || (absorb && BT <= 128)) return 64;
   return 128;
 }
 
@@ -413,7 +418,7 @@ cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q, in
                           int32_t* status, cudaStream_t st, const uint8_t* wuk8,
                           const float* wuk_scale) {
   const Fp8Weights w8{wuk8, wuk_scale, kLora};
-  switch (bmm_token_tile(BT)) {
+  switch (bmm_token_tile(BT, true)) {
     case 16: return launch_bmm_nt<BmmMode::kAbsorb, 16>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st, w8);
     case 32: return launch_bmm_nt<BmmMode::kAbsorb, 32>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st, w8);
     case 64: return launch_bmm_nt<BmmMode::kAbsorb, 64>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st, w8);
@@ -425,7 +430,7 @@ cudaError_t launch_up_project(const CUtensorMap& tm_wuv, const CUtensorMap& tm_o
                               int H, __nv_bfloat16* out, int32_t* status, cudaStream_t st,
                               const uint8_t* wuv8, const float* wuv_scale) {
   const Fp8Weights w8{wuv8, wuv_scale, kVHead};
-  switch (bmm_token_tile(BT)) {
+  switch (bmm_token_tile(BT, false)) {
     case 16: return launch_bmm_nt<BmmMode::kUpProject, 16>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);
     case 32: return launch_bmm_nt<BmmMode::kUpProject, 32>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);
     case 64: return launch_bmm_nt<BmmMode::kUpProject, 64>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);
