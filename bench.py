@@ -244,6 +244,10 @@ def run_reference(args):
         return
     import oracle
     inp = workload_inputs(args.workload)
+    if args.weights == "fp8":  # the oracle decompresses the FP8 weights, then decodes
+        from mla_decode_attention_uk_gb300.inputs import quantize_fp8_blockwise
+        inp.w_uk = oracle.dequant_fp8_weight(*quantize_fp8_blockwise(inp.w_uk))
+        inp.w_uv = oracle.dequant_fp8_weight(*quantize_fp8_blockwise(inp.w_uv))
     budget = min(1.0, 120.0 / max(1, args.steps + args.warmup))
     rows, nbytes, flops, tokens, text = oracle_sample(inp, budget)
     times = []
@@ -260,7 +264,9 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "note": WORKLOADS[args.workload].note},
+        "config": {"workload": args.workload, "note": WORKLOADS[args.workload].note,
+                   "weights": "fp8 e4m3, 128x128 block scales" if args.weights == "fp8"
+                   else "bf16"},
         "tflops": flops / per_step / 1e12, "tokens_per_s": tokens / per_step,
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.threads(),
                          "kind": "oracle", "sample": text},
