@@ -13,20 +13,23 @@
 // A = a 128-wide slice of W[h] (MN-major, staged by TMA with 128B swizzle),
 // B = a token tile of X (K-major), D in TMEM (fp32), one CTA per
 // (token tile, 128-wide m block, head).  Warp 0 issues TMA, warp 1 issues the
-// MMAs, warp 2 owns TMEM, and all four warps run the epilogue.
+// MMAs, warp 2 owns TMEM; warps 0-3 move the accumulator out of TMEM and all
+// warps store the tile.
 //
 // The absorb epilogue also writes the bf16 residual q_lat - bf16(q_lat), which
-// the attention step uses to correct its log-sum-exp to first order.
+// the attention step uses to correct its log-sum-exp to first order; the
+// q_pe columns of q_lat are copied by the warps not busy with TMA or MMAs
+// while the MMAs run.
 //
 // FP8 weights (W8): the page says the absorbed form lacks an FP8 bmm, so the
 // matrices involved are decompressed to bf16 and the bmm runs in bf16.  Here
 // the decompression happens inside the bmm: W is stored as FP8 E4M3 with one
-// fp32 scale per 128 x 128 block.  Warps 2-3 keep a ring of raw 64 x 128 FP8
-// tiles filled by TMA (issued before the kernel waits for its predecessor:
-// the weights do not depend on it), form W = bf16(fp32(w8) * scale) (fp32
-// product, round to nearest even) and write it straight into the swizzled
-// shared-memory layout the MMA reads, while warp 0 brings the activation tile.
-// FP8 kernels run 192 threads: warps 2-5 convert.
+// fp32 scale per 128 x 128 block.  FP8 kernels run 192 threads: warps 2-5
+// keep a ring of raw 64 x 128 FP8 tiles filled by TMA (issued before the
+// kernel waits for its predecessor: the weights do not depend on it), form
+// W = bf16(fp32(w8) * scale) (fp32 product, round to nearest even) and write
+// it straight into the swizzled shared-memory layout the MMA reads, while
+// warp 0 brings the activation tile.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -41,7 +44,7 @@ namespace mla {
 namespace {
 
 constexpr int kBmmThreads = 128;    // bf16 weights
-constexpr int kBmmThreadsW8 = 192;  // FP8 weights: four converter warps more
+constexpr int kBmmThreadsW8 = 192;  // FP8 weights: two warps more (2-5 convert)
 constexpr int kABytes = 2 * kBoxBytes;  // 128 m x 64 k, two 64-wide m boxes
 
 enum class BmmMode { kAbsorb, kUpProject };
