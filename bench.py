@@ -92,6 +92,27 @@ def workload_stats(inp, fp8_weights=False):
                 tokens=B * T)
 
 
+def attention_roofline(stats, attend_s, hbm, bf16, peak_src, traffic):
+    """Roofline object of the attention kernel (the dominant one): bound by
+    the slower of streaming the latent cache at the measured copy bandwidth
+    (GB/s) and its FLOPs at the measured bf16 peak (TF/s); achieved figures
+    are algorithmic bytes / FLOPs over the kernel's average launch time."""
+    attend_gbs = stats["cache_bytes"] / attend_s / 1e9
+    attend_tf = stats["attn_flops"] / attend_s / 1e12
+    if stats["attn_flops"] / (bf16 * 1e12) > stats["cache_bytes"] / (hbm * 1e9):
+        roof = {"bound": "tensor", "achieved": attend_tf, "peak": bf16, "unit": "TFLOP/s",
+                "frac": attend_tf / bf16,
+                "peak_source": peak_src + " (bf16_tflops, MEASURED_PEAKS.json)"}
+    else:
+        roof = {"bound": "hbm", "achieved": attend_gbs, "peak": hbm, "unit": "GB/s",
+                "frac": attend_gbs / hbm,
+                "peak_source": peak_src + " (hbm_gbs, MEASURED_PEAKS.json)"}
+    roof.update({"traffic": traffic, "kernel": "decode_kernel (attend step)",
+                 "kernel_us": attend_s * 1e6, "hbm_frac": attend_gbs / hbm,
+                 "tensor_frac": attend_tf / bf16})
+    return roof
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled in the background."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -489,20 +510,7 @@ def main():
     hbm, bf16, bf16_sus, peak_src = measured_peaks()
     gbs = world * stats["cache_bytes"] / per_step / 1e9
     tflops = world * stats["flops"] / per_step / 1e12
-    attend_gbs = stats["cache_bytes"] / attend_s / 1e9
-    attend_tf = stats["attn_flops"] / attend_s / 1e12
-    traffic = ncu_traffic(args.workload)
-    # The attention kernel's own roofline: the slower of streaming the cache at
-    # the measured copy bandwidth and its FLOPs at the measured bf16 peak.
-    if stats["attn_flops"] / (bf16 * 1e12) > stats["cache_bytes"] / (hbm * 1e9):
-        roof = {"bound": "tensor", "achieved": attend_tf, "peak": bf16, "unit": "TFLOP/s",
-                "frac": attend_tf / bf16, "peak_source": peak_src + " (bf16_tflops, MEASURED_PEAKS.json)"}
-    else:
-        roof = {"bound": "hbm", "achieved": attend_gbs, "peak": hbm, "unit": "GB/s",
-                "frac": attend_gbs / hbm, "peak_source": peak_src + " (hbm_gbs, MEASURED_PEAKS.json)"}
-    roof.update({"traffic": traffic, "kernel": "decode_kernel (attend step)",
-                 "kernel_us": attend_s * 1e6, "hbm_frac": attend_gbs / hbm,
-                 "tensor_frac": attend_tf / bf16})
+    roof = attention_roofline(stats, attend_s, hbm, bf16, peak_src, ncu_traffic(args.workload))
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
