@@ -36,7 +36,9 @@ def _max_worker(rank, world, port, results):
 
 def test_max_over_ranks_gloo_world2():
     port = _free_port()
-    with mp.Manager() as mgr:
+    # The manager's server process starts with spawn too: forking a process
+    # whose threads (torch, OpenMP) are already running can deadlock.
+    with mp.get_context("spawn").Manager() as mgr:
         results = mgr.dict()
         mp.spawn(_max_worker, args=(2, port, results), nprocs=2, join=True)
         assert dict(results) == {0: 2.5, 1: 2.5}
