@@ -149,9 +149,10 @@ int mla_decode_combine(const mla_decode_dims* dims, float softmax_scale, float* 
 int mla_decode_up_project(const mla_decode_dims* dims, const void* w_uv, void* out,
                           void* workspace, size_t workspace_bytes, void* stream);
 
-/* The same steps with FP8 weights.  The page says the absorbed form has no FP8
- * bmm, so the weights are decompressed to bf16 and the bmm runs in bf16; here
- * the bmm kernels decompress each weight tile as they load it.
+/* The same steps with FP8 weights.  vLLM PR #14770 "[Attention] MLA get rid
+ * of materialization" (PR description) notes that the absorbed form has no
+ * FP8 bmm, so FP8 weights are decompressed to bf16 and the bmm runs in bf16;
+ * here the bmm kernels decompress each weight tile as they load it.
  *   w_uk_fp8    uint8 [H, 128, 512]  FP8 E4M3 (4-bit exponent, bias 7, 3-bit
  *               mantissa, no infinities; S.1111.111 is NaN)
  *   w_uk_scale  fp32  [H, 1, 4]      one scale per 128 x 128 block (k, m)

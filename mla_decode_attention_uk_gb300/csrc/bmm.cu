@@ -21,8 +21,8 @@
 // q_pe columns of q_lat are copied by the warps not busy with TMA or MMAs
 // while the MMAs run.
 //
-// FP8 weights (W8): the page says the absorbed form lacks an FP8 bmm, so the
-// matrices involved are decompressed to bf16 and the bmm runs in bf16.  Here
+// FP8 weights (W8): the same PR description notes that the absorbed form has
+// no FP8 bmm, so FP8 weights are decompressed to bf16 and the bmm runs in bf16.  Here
 // the decompression happens inside the bmm: W is stored as FP8 E4M3 with one
 // fp32 scale per 128 x 128 block.  FP8 kernels run 192 threads: warps 2-5
 // keep a ring of raw 64 x 128 FP8 tiles filled by TMA (issued before the

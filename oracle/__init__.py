@@ -147,9 +147,10 @@ def default_scale(qk_nope=128, qk_rope=64):
 # above then applies unchanged.
 
 def e4m3_to_float(codes):
-    """Values of FP8 E4M3 codes (uint8 array): sign bit, 4-bit exponent with
-    bias 7, 3-bit mantissa; exponent 0 is subnormal (m/8 * 2^-6); no
-    infinities; S.1111.111 is NaN.  Returns float64."""
+    """Values of FP8 E4M3 codes (uint8 array), the E4M3 encoding of the OCP
+    8-bit floating-point formats: sign bit, 4-bit exponent with bias 7, 3-bit
+    mantissa; exponent 0 is subnormal (m/8 * 2^-6); no infinities; S.1111.111
+    is NaN.  Returns float64."""
     c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
     sign = np.where(c & 0x80, -1.0, 1.0)
     e = (c >> 3) & 0xF
@@ -162,7 +163,11 @@ def e4m3_to_float(codes):
 
 def dequant_fp8_weight(w8, scale):
     """bf16 weight [H, K, M] from E4M3 codes w8 (uint8 [H, K, M]) and fp32 block
-    scales [H, K/128, M/128]: bf16(fp32(value) * fp32(scale))."""
+    scales [H, K/128, M/128]: bf16(fp32(value) * fp32(scale)).  The
+    decompression to bf16 that vLLM PR #14770 "[Attention] MLA get rid of
+    materialization" (PR description) applies to FP8 weights, since the
+    absorbed form has no FP8 bmm; the block-scale layout is this library's
+    reading of "FP8 weights"."""
     w8 = torch.as_tensor(w8)
     H, K, M = w8.shape
     vals = torch.from_numpy(e4m3_to_float(w8.numpy()).astype(np.float32))  # exact in fp32
