@@ -146,3 +146,36 @@ def test_fp8_step_calls_check_their_scales():
                                         1 << 30, None) == 1
     assert L.mla_decode_up_project_fp8w(ctypes.byref(d), ok, ok, ok, ok, 64, None) == 3
 
+
+
+@pytest.mark.parametrize("B,T,H,R", [(2, 1, 16, 5), (64, 1, 16, 152), (256, 2, 128, 38),
+                                     (64, 8, 128, 9), (5000, 1, 16, 152), (1, 1, 48, 1)])
+def test_workspace_layout_holds_the_documented_buffers(B, T, H, R):
+    # With an explicit range count the sizing needs no device.  The header
+    # documents q_lat bf16 [B*T*H, 576], q_lo and o_lat bf16 [B*T*H, 512];
+    # the split partials (two slots per range: fp32 lse [T*H] and o [T*H, 512]
+    # each) come after them.
+    L = binding.lib()
+    d = good_dims(batch=B, q_len=T, num_heads=H)
+    n = ctypes.c_size_t(0)
+    assert L.mla_decode_workspace_size_ex(ctypes.byref(d), R, ctypes.byref(n)) == 0
+    off = (ctypes.c_int64 * 4)()
+    assert L.mla_decode_workspace_offsets(ctypes.byref(d), R, off, 4) == 0
+    q_lat, q_lo, o_lat, header = off
+    rows = B * T * H
+    assert all(o % 16 == 0 for o in off)
+    assert header + 16 <= q_lat  # plan header (four int32) before the buffers
+    assert q_lat + rows * 576 * 2 <= q_lo
+    assert q_lo + rows * 512 * 2 <= o_lat
+    partials = 2 * R * T * H * (512 + 1) * 4
+    assert o_lat + rows * 512 * 2 + partials <= n.value
+    # Each extra range adds two partial slots (and its range bounds): at least
+    # the two fp32 [T*H, 512] outputs; the small arrays may fit in the 256-byte
+    # rounding of their regions.
+    n2 = ctypes.c_size_t(0)
+    assert L.mla_decode_workspace_size_ex(ctypes.byref(d), R + 1, ctypes.byref(n2)) == 0
+    grow = n2.value - n.value
+    assert 2 * T * H * 512 * 4 <= grow <= 2 * T * H * (512 + 1) * 4 + 4 * 256
+    # Without a device the default range count cannot be known.
+    assert L.mla_decode_workspace_size_ex(ctypes.byref(d), -1, ctypes.byref(n2)) == 1
+    assert L.mla_decode_workspace_size_ex(ctypes.byref(d), 65537, ctypes.byref(n2)) == 1
