@@ -24,7 +24,7 @@ cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q, in
                           const float* wuk_scale);
 cudaError_t launch_up_project(const CUtensorMap& tm_wuv, const CUtensorMap& tm_olat, int BT,
                               int H, __nv_bfloat16* out, int32_t* status, cudaStream_t st,
-                              const uint8_t* wuv8, const float* wuv_scale);
+                              const uint8_t* wuv8, const float* wuv_scale, bool one_wave);
 int decode_tiles(int T, int H);
 int decode_q_box_rows(int T, int H);
 cudaError_t decode_max_groups(int T, int H, int sm_count, int* groups);
@@ -38,7 +38,7 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
 cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, const void* ws,
                            const PlanHeader* header, const __nv_bfloat16* qlo,
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
-                           bool many_splits, cudaStream_t st);
+                           int splits_per_seq, cudaStream_t st);
 }  // namespace mla
 
 namespace {
@@ -321,9 +321,14 @@ static int up_project_impl(const mla_decode_dims* d, const void* w_uv, const uin
            : make_map(&tm_w, w_uv, static_cast<uint64_t>(H) * kLora, kVHead, kVHead, kBoxCols, 64,
                       false)))
     return MLA_DECODE_CUDA_ERROR;
+  int sms = 0;
+  rc = sm_count(&sms);
+  if (rc) return rc;
+  const int nt = bmm_token_tile(BT, false);
+  const bool one_wave = static_cast<int64_t>((BT + nt - 1) / nt) * H <= sms;
   return cuda_rc(launch_up_project(tm_w, tm_o, BT, H, static_cast<__nv_bfloat16*>(out),
                                    at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream),
-                                   w8, w8_scale));
+                                   w8, w8_scale, one_wave));
 }
 
 int mla_decode_absorb(const mla_decode_dims* d, const void* q, const void* w_uk, void* ws,
@@ -378,16 +383,17 @@ int mla_decode_combine(const mla_decode_dims* d, float scale, float* lse, void* 
   WsLayout L;
   rc = layout_for(d, ws_bytes, &L);
   if (rc) return rc;
-  // With at least as many work ranges as sequences, sequences are typically
-  // cut into several splits; with fewer, most rows are unsplit.  (Only the
-  // speed depends on this guess: both combine variants compute the same.)
+  // With fewer work ranges than sequences most rows are unsplit; otherwise a
+  // sequence is typically cut into about ranges / batch splits.  (Only the
+  // speed depends on this guess: every combine variant computes the same.)
   int ranges = 0;
   rc = default_ranges(d, &ranges);
   if (rc) return rc;
+  const int splits_per_seq = ranges < d->batch ? 1 : (ranges + d->batch - 1) / d->batch;
   return cuda_rc(launch_combine(at<int32_t>(ws, L.seq_nsplit), at<int32_t>(ws, L.seq_slot), ws,
                                 at<PlanHeader>(ws, L.header), at<__nv_bfloat16>(ws, L.qlo),
                                 at<__nv_bfloat16>(ws, L.olat), lse, d->batch, d->q_len,
-                                d->num_heads, scale, ranges >= d->batch,
+                                d->num_heads, scale, splits_per_seq,
                                 static_cast<cudaStream_t>(stream)));
 }
 

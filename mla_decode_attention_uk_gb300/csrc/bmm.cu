@@ -381,14 +381,16 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   if constexpr (MODE == BmmMode::kAbsorb) griddep_wait();
 }
 
-template <BmmMode MODE, int NT>
+template <BmmMode MODE, int NT, int kStagesAll = 0>
 cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, int H, int K,
                           int Kx, int Mtot, const __nv_bfloat16* q, __nv_bfloat16* hi,
                           __nv_bfloat16* lo, int32_t* status, cudaStream_t st,
                           Fp8Weights w8) {
   // Two stages for the absorb step (K = 128) and for 128-token tiles (64 KB of
-  // stages, three CTAs per SM); four for the up-projection's smaller tiles.
-  constexpr int STAGES = (MODE == BmmMode::kAbsorb || NT == 128) ? 2 : 4;
+  // stages, three CTAs per SM); four for the up-projection's smaller tiles,
+  // or kStagesAll (all of K) when the caller asks for it.
+  constexpr int STAGES =
+      kStagesAll ? kStagesAll : ((MODE == BmmMode::kAbsorb || NT == 128) ? 2 : 4);
   auto kern = w8.w ? bmm_kernel<MODE, NT, STAGES, true> : bmm_kernel<MODE, NT, STAGES, false>;
   const int smem = w8.w ? BmmSmem<NT, STAGES, raw_tiles(MODE, true)>::kTotal
                         : BmmSmem<NT, STAGES, 0>::kTotal;
@@ -431,8 +433,20 @@ cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q, in
 
 cudaError_t launch_up_project(const CUtensorMap& tm_wuv, const CUtensorMap& tm_olat, int BT,
                               int H, __nv_bfloat16* out, int32_t* status, cudaStream_t st,
-                              const uint8_t* wuv8, const float* wuv_scale) {
+                              const uint8_t* wuv8, const float* wuv_scale, bool one_wave) {
   const Fp8Weights w8{wuv8, wuv_scale, kVHead};
+  // When the whole grid runs in one wave, tiles of up to 64 tokens get a stage
+  // for each of the eight 64-deep K steps (up to 225 KB of shared memory, one
+  // CTA per SM): every o_lat tile loads at once after the wait, and FP8
+  // weights are decompressed before o_lat is ready, behind the combine step.
+  if (one_wave) {
+    switch (bmm_token_tile(BT, false)) {
+      case 16: return launch_bmm_nt<BmmMode::kUpProject, 16, 8>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);
+      case 32: return launch_bmm_nt<BmmMode::kUpProject, 32, 8>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);
+      case 64: return launch_bmm_nt<BmmMode::kUpProject, 64, 8>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);
+      default: break;
+    }
+  }
   switch (bmm_token_tile(BT, false)) {
     case 16: return launch_bmm_nt<BmmMode::kUpProject, 16>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);
     case 32: return launch_bmm_nt<BmmMode::kUpProject, 32>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);

@@ -14,11 +14,14 @@
 // scale * (q_lo . o) restores the scores of the full-precision query up to
 // second order in q_lo (|q_lo| <= 2^-9 |q_lat|).
 // One warp per query row; each lane owns 16 of the 512 latent columns and
-// moves them with 16-byte vector loads.  Two instantiations differ in how far
-// the loop over a row's splits is unrolled: by 4 when sequences are cut into
-// many splits (more loads in flight per warp), or not at all when most rows
-// are unsplit (64 registers instead of 70, so four CTAs fit on an SM instead
-// of three).
+// moves them with 16-byte vector loads.  Three instantiations:
+//   - split loop not unrolled, when most rows are unsplit (64 registers, four
+//     CTAs per SM);
+//   - unrolled by 4, when sequences are cut into many splits (more loads in
+//     flight per warp);
+//   - unrolled by 4 plus a path for rows of at most 4 splits that loads every
+//     split's partial output together with its lse (one memory round trip
+//     instead of two), when sequences are cut into a few splits.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -32,7 +35,7 @@ namespace {
 constexpr int kCombThreads = 256;
 constexpr int kRowsPerCta = kCombThreads / 32;
 
-template <int kUnroll>
+template <int kUnroll, bool kFew>
 __global__ void __launch_bounds__(kCombThreads)
 combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict__ seq_slot,
                const uint8_t* __restrict__ ws, const PlanHeader* __restrict__ header, int B,
@@ -88,46 +91,81 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
   const float* __restrict__ opart = reinterpret_cast<const float*>(ws + L.opart);
   const float* __restrict__ lpart = reinterpret_cast<const float*>(ws + L.lpart);
 
-  // Lane s holds the lse of split s (32 splits per pass), so the loads go out
-  // together and the max and sum are warp reductions.
-  float m = -INFINITY;
-  for (int s0 = 0; s0 < ns; s0 += 32) {
-    const float l = s0 + lane < ns ? lpart[static_cast<size_t>(slot0 + s0 + lane) * TH + r]
-                                   : -INFINITY;
-    m = fmaxf(m, l);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float wsum = 0.0f;
-  for (int s0 = 0; s0 < ns; s0 += 32) {
-    const float l = s0 + lane < ns ? lpart[static_cast<size_t>(slot0 + s0 + lane) * TH + r]
-                                   : -INFINITY;
-    wsum += (l == -INFINITY) ? 0.0f : __expf(l - m);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-  const float lse = m + __logf(wsum);
-
   float4 acc[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < ns; s0 += 32) {
-    const float l = s0 + lane < ns ? lpart[static_cast<size_t>(slot0 + s0 + lane) * TH + r]
-                                   : -INFINITY;
-    const float wl = (l == -INFINITY) ? 0.0f : __expf(l - lse);  // weight of split s0 + lane
-    const int n = min(32, ns - s0);
-#pragma unroll kUnroll
-    for (int i = 0; i < n; ++i) {
-      const float w = __shfl_sync(0xffffffffu, wl, i);
-      const float4* src = reinterpret_cast<const float4*>(
-          opart + (static_cast<size_t>(slot0 + s0 + i) * TH + r) * kLora);
+  float lse;
+  if (kFew && ns <= 4) {
+    // Every split's lse and partial output go out at once.
+    float l[4];
+    float4 v[4][4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = src[q * 32 + lane];
-        acc[q].x += w * v.x;
-        acc[q].y += w * v.y;
-        acc[q].z += w * v.z;
-        acc[q].w += w * v.w;
+    for (int s = 0; s < 4; ++s) {
+      l[s] = -INFINITY;
+      if (s < ns) {
+        const size_t srow = static_cast<size_t>(slot0 + s) * TH + r;
+        l[s] = lpart[srow];
+        const float4* src = reinterpret_cast<const float4*>(opart + srow * kLora);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[s][q] = src[q * 32 + lane];
+      }
+    }
+    const float m = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
+    float wsum = 0.0f;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) wsum += (l[s] == -INFINITY) ? 0.0f : __expf(l[s] - m);
+    lse = m + __logf(wsum);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      if (s < ns) {
+        const float w = (l[s] == -INFINITY) ? 0.0f : __expf(l[s] - lse);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[q].x += w * v[s][q].x;
+          acc[q].y += w * v[s][q].y;
+          acc[q].z += w * v[s][q].z;
+          acc[q].w += w * v[s][q].w;
+        }
+      }
+    }
+  } else {
+    // Lane s holds the lse of split s (32 splits per pass), so the loads go
+    // out together and the max and sum are warp reductions.
+    float m = -INFINITY;
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      const float l = s0 + lane < ns ? lpart[static_cast<size_t>(slot0 + s0 + lane) * TH + r]
+                                     : -INFINITY;
+      m = fmaxf(m, l);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float wsum = 0.0f;
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      const float l = s0 + lane < ns ? lpart[static_cast<size_t>(slot0 + s0 + lane) * TH + r]
+                                     : -INFINITY;
+      wsum += (l == -INFINITY) ? 0.0f : __expf(l - m);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    lse = m + __logf(wsum);
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      const float l = s0 + lane < ns ? lpart[static_cast<size_t>(slot0 + s0 + lane) * TH + r]
+                                     : -INFINITY;
+      const float wl = (l == -INFINITY) ? 0.0f : __expf(l - lse);  // weight of split s0 + lane
+      const int n = min(32, ns - s0);
+#pragma unroll kUnroll
+      for (int i = 0; i < n; ++i) {
+        const float w = __shfl_sync(0xffffffffu, wl, i);
+        const float4* src = reinterpret_cast<const float4*>(
+            opart + (static_cast<size_t>(slot0 + s0 + i) * TH + r) * kLora);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 v = src[q * 32 + lane];
+          acc[q].x += w * v.x;
+          acc[q].y += w * v.y;
+          acc[q].z += w * v.z;
+          acc[q].w += w * v.w;
+        }
       }
     }
   }
@@ -157,9 +195,13 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
 cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, const void* ws,
                            const PlanHeader* header, const __nv_bfloat16* qlo,
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
-                           bool many_splits, cudaStream_t st) {
+                           int splits_per_seq, cudaStream_t st) {
   dim3 grid((T * H + kRowsPerCta - 1) / kRowsPerCta, B);
-  auto kern = many_splits ? combine_kernel<4> : combine_kernel<1>;
+  // splits_per_seq: work ranges per sequence, rounded up (the host's guess of
+  // the typical split count; only the speed depends on it).
+  auto kern = splits_per_seq <= 1   ? combine_kernel<1, false>
+              : splits_per_seq <= 4 ? combine_kernel<4, true>
+                                    : combine_kernel<4, false>;
   cudaError_t e = launch_pdl(kern, grid, dim3(kCombThreads), 0, st, seq_nsplit, seq_slot,
                              static_cast<const uint8_t*>(ws), header, B, T, H, qlo, olat, lse,
                              scale);
