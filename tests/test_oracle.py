@@ -425,3 +425,25 @@ def test_fp8_dequant_rounds_to_nearest_even_bf16_and_uses_block_scales():
     d = oracle.dequant_fp8_weight(w8, scale).double()
     assert torch.all(d[0, :128] == 2.0) and torch.all(d[0, 128:] == 4.0)
     assert torch.all(d[1, :128] == 8.0) and torch.all(d[1, 128:] == 0.5)
+
+
+def test_fp8_test_weights_round_trip_within_e4m3_precision():
+    # The FP8 test inputs: per-block scale = amax / 448, codes rounded to the
+    # nearest E4M3 value.  Decompressed, each weight is within half an E4M3
+    # step of the original (relative 2^-4 for normal values, 2^-10 of the
+    # scale in the subnormal range, plus the bf16 rounding), and each block's
+    # largest magnitude maps to code 448.
+    from mla_decode_attention_uk_gb300.inputs import make_inputs, quantize_fp8_blockwise
+    inp = make_inputs(1, [5], 1, 16, seed=91)
+    for w in (inp.w_uk, inp.w_uv):
+        codes, scale = quantize_fp8_blockwise(w)
+        d = oracle.dequant_fp8_weight(codes, scale).double()
+        H, K, M = w.shape
+        s = scale.double().repeat_interleave(128, 1).repeat_interleave(128, 2)
+        err = (d - w.double()).abs()
+        bound = torch.maximum(w.double().abs() * 2.0 ** -4, s * 2.0 ** -10) * 1.01 + \
+            d.abs() * 2.0 ** -8
+        assert torch.all(err <= bound)
+        vals = torch.from_numpy(oracle.e4m3_to_float(codes.numpy()))
+        blockmax = vals.abs().reshape(H, K // 128, 128, M // 128, 128).amax(dim=(2, 4))
+        assert torch.all(blockmax == 448.0)
