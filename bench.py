@@ -12,7 +12,12 @@ HBM copy bandwidth, an end-to-end figure through the same C ABI with host
 buffers, and the fp64 CPU oracle timed on a bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
-                  [--weights bf16|fp8]
+                  [--weights bf16|fp8] [--no-per-config]
+
+The attention kernel's time (the roofline's "achieved") is always taken over
+ATTEND_LAUNCHES back-to-back launches, whatever --steps is.  "per_config"
+repeats the step and attention timing (CONFIG_STEPS steps, ATTEND_LAUNCHES
+launches) on every full-size workload, so one line carries all of them.
 
 --weights fp8 gives the two bmms W_UK and W_UV as FP8 E4M3 codes with one
 fp32 scale per 128 x 128 block (decompressed to bf16 inside the bmm kernels).
@@ -37,8 +42,14 @@ import torch  # noqa: E402
 from mla_decode_attention_uk_gb300.inputs import WORKLOADS, workload_inputs  # noqa: E402
 
 METRIC = "MLA decode latent-KV GB/s, TFLOPS & tokens/s vs GB300 roofline (1 GPU)"
-DEFAULT_WORKLOAD = "tp_shard"
+# The headline runs on the largest single-GPU workload (811 MB of latent
+# cache, ~200 GFLOP per step); every other full-size workload is measured in
+# the same run and reported under "per_config".
+DEFAULT_WORKLOAD = "full_head"
+PER_CONFIG = ("tp_shard", "long", "full_head", "mixed_spec", "draft_q8")
 PER_GRAPH = 10  # decode steps captured in one CUDA graph replay
+ATTEND_LAUNCHES = 300  # back-to-back launches that time the attention kernel
+CONFIG_STEPS = 300  # graph-replayed steps that time each per-config workload
 BYTES_PER_TOKEN = 1152          # 576 bf16 per cached token
 FLOP_PER_ROW_KEY = 2 * (576 + 512)
 FLOP_PER_ROW_BMM = 2 * 2 * 128 * 512
@@ -298,16 +309,169 @@ def run_reference(args):
         dist.destroy_process_group()
 
 
+class WorkloadRunner:
+    """One workload's inputs on the device, a workspace through the binding,
+    and CUDA graphs of PER_GRAPH consecutive decode steps and of PER_GRAPH
+    attention launches (same kernels and arguments as host launches; the
+    graphs keep host launch overhead from starving the GPU on small batches)."""
+
+    def __init__(self, name, dev, fp8, use_graph=True):
+        from mla_decode_attention_uk_gb300 import binding
+        self.binding = binding
+        self.name = name
+        self.dev = dev
+        self.fp8 = fp8
+        self.inp_cpu = workload_inputs(name)
+        self.stats = workload_stats(self.inp_cpu, fp8)
+        g = self.g = self.inp_cpu.to(dev)
+        if fp8:
+            from mla_decode_attention_uk_gb300.inputs import quantize_fp8_blockwise
+            uk8, uk_s = quantize_fp8_blockwise(self.inp_cpu.w_uk)
+            uv8, uv_s = quantize_fp8_blockwise(self.inp_cpu.w_uv)
+            self.wts = {k: (t, t.to(dev)) for k, t in (("uk8", uk8), ("uk_s", uk_s),
+                                                       ("uv8", uv8), ("uv_s", uv_s))}
+        else:
+            self.wts = {"w_uk": (self.inp_cpu.w_uk, g.w_uk), "w_uv": (self.inp_cpu.w_uv, g.w_uv)}
+        self.W = {k: v[1] for k, v in self.wts.items()}
+        self.m = binding.MlaDecode(binding.dims_for(g.q, g.cache, g.block_table), dev)
+        B, T, H = self.stats["B"], self.stats["T"], self.stats["H"]
+        self.out = torch.empty(B, T, H, 128, dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty(B, T, H, dtype=torch.float32, device=dev)
+        self.use_graph = use_graph
+        self.graph_step = self.graph_attend = None
+
+    # -- the path, one call per step of it
+    def absorb(self):
+        if self.fp8:
+            self.m.absorb_fp8w(self.g.q, self.W["uk8"], self.W["uk_s"])
+        else:
+            self.m.absorb(self.g.q, self.W["w_uk"])
+
+    def attend(self):
+        g = self.g
+        self.m.attend(g.cache, g.block_table, g.seq_lens, g.scale, self.lse)
+
+    def combine(self):
+        self.m.combine(self.g.scale, self.lse)
+
+    def up_project(self):
+        if self.fp8:
+            self.m.up_project_fp8w(self.W["uv8"], self.W["uv_s"], self.out)
+        else:
+            self.m.up_project(self.W["w_uv"], self.out)
+
+    def plan(self):
+        self.m.plan(self.g.seq_lens)
+
+    def step(self):
+        self.plan()
+        self.absorb()
+        self.attend()
+        self.combine()
+        self.up_project()
+
+    def run_all(self):
+        g, W = self.g, self.W
+        if self.fp8:
+            self.m.run_fp8w(g.q, g.cache, g.block_table, g.seq_lens, W["uk8"], W["uk_s"], W["uv8"],
+                            W["uv_s"], g.scale, self.out, self.lse)
+        else:
+            self.m.run(g.q, g.cache, g.block_table, g.seq_lens, W["w_uk"], W["w_uv"], g.scale,
+                       self.out, self.lse)
+
+    def check(self, where):
+        st = self.m.check()
+        if st != 0:
+            raise SystemExit("%s: device status %d %s" % (self.name, st, where))
+
+    def prepare(self, warmup):
+        stream = torch.cuda.current_stream()
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        self.check("after warm-up")
+        if not self.use_graph:
+            return
+        side = torch.cuda.Stream(self.dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            self.step()
+            self.attend()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph_step, self.graph_attend = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph_step):
+            for _ in range(PER_GRAPH):
+                self.step()
+        with torch.cuda.graph(self.graph_attend):
+            for _ in range(PER_GRAPH):
+                self.attend()
+        torch.cuda.synchronize()
+        for _ in range(max(1, warmup // PER_GRAPH)):
+            self.graph_step.replay()
+        torch.cuda.synchronize()
+
+    def per_call(self):
+        return PER_GRAPH if self.graph_step is not None else 1
+
+    def steps_call(self):
+        return self.graph_step.replay if self.graph_step is not None else self.step
+
+    def attends_call(self):
+        return self.graph_attend.replay if self.graph_attend is not None else self.attend
+
+    def time_calls(self, fn, calls):
+        """Seconds per call of fn over `calls` back-to-back calls (CUDA events
+        on the launching stream, synchronised on both sides)."""
+        stream = torch.cuda.current_stream()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(calls):
+            fn()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / 1e3 / calls
+
+    def time_attend(self, launches=ATTEND_LAUNCHES):
+        """Average attention-kernel launch time over `launches` back-to-back
+        launches (inputs larger than L2: every launch streams the cache)."""
+        n = max(1, launches // self.per_call())
+        return self.time_calls(self.attends_call(), n) / self.per_call(), n * self.per_call()
+
+    def free(self):
+        self.graph_step = self.graph_attend = None
+        self.g = self.W = self.wts = self.m = self.out = self.lse = None
+
+
+def per_config_entry(r, step_s, attend_s, attend_launches, hbm, bf16, peak_src):
+    st = r.stats
+    roof = attention_roofline(st, attend_s, hbm, bf16, peak_src, ncu_traffic(r.name))
+    return {
+        "note": WORKLOADS[r.name].note, "step_us": step_s * 1e6,
+        "value_gbs": st["cache_bytes"] / step_s / 1e9, "tflops": st["flops"] / step_s / 1e12,
+        "tokens_per_s": st["tokens"] / step_s,
+        "attend_us": attend_s * 1e6, "attend_launches": attend_launches,
+        "bound": roof["bound"], "frac": roof["frac"], "hbm_frac": roof["hbm_frac"],
+        "tensor_frac": roof["tensor_frac"], "traffic": roof["traffic"],
+        "cache_bytes": st["cache_bytes"], "attn_flops": st["attn_flops"],
+        "t_roof_us": 1e6 * max((st["cache_bytes"] + st["weight_bytes"]) / (hbm * 1e9),
+                               st["flops"] / (bf16 * 1e12)),
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=30)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch every step from the host")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure only --workload (e.g. for short profiler runs)")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "fp8"],
                     help="W_UK / W_UV as bf16, or FP8 E4M3 with 128x128 block scales")
     ap.add_argument("--breakdown", action="store_true",
@@ -323,96 +487,24 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
-
-    inp_cpu = workload_inputs(args.workload)
     fp8 = args.weights == "fp8"
-    stats = workload_stats(inp_cpu, fp8)
-    g = inp_cpu.to(dev)
-    # Weight operands of the two bmms: name -> (host tensor, device tensor).
-    if fp8:
-        from mla_decode_attention_uk_gb300.inputs import quantize_fp8_blockwise
-        uk8, uk_s = quantize_fp8_blockwise(inp_cpu.w_uk)
-        uv8, uv_s = quantize_fp8_blockwise(inp_cpu.w_uv)
-        wts = {k: (t, t.to(dev)) for k, t in (("uk8", uk8), ("uk_s", uk_s), ("uv8", uv8),
-                                              ("uv_s", uv_s))}
-    else:
-        wts = {"w_uk": (inp_cpu.w_uk, g.w_uk), "w_uv": (inp_cpu.w_uv, g.w_uv)}
-    W = {k: v[1] for k, v in wts.items()}
+    hbm, bf16, bf16_sus, peak_src = measured_peaks()
 
-    def absorb():
-        if fp8:
-            m.absorb_fp8w(g.q, W["uk8"], W["uk_s"])
-        else:
-            m.absorb(g.q, W["w_uk"])
-
-    def up_project():
-        if fp8:
-            m.up_project_fp8w(W["uv8"], W["uv_s"], out)
-        else:
-            m.up_project(W["w_uv"], out)
-
-    def run_all():
-        if fp8:
-            m.run_fp8w(g.q, g.cache, g.block_table, g.seq_lens, W["uk8"], W["uk_s"], W["uv8"],
-                       W["uv_s"], g.scale, out, lse)
-        else:
-            m.run(g.q, g.cache, g.block_table, g.seq_lens, W["w_uk"], W["w_uv"], g.scale, out, lse)
-    d = binding.dims_for(g.q, g.cache, g.block_table)
-    m = binding.MlaDecode(d, dev)
+    r = WorkloadRunner(args.workload, dev, fp8, use_graph=not args.no_graph)
+    stats, inp_cpu, g = r.stats, r.inp_cpu, r.g
     B, T, H = stats["B"], stats["T"], stats["H"]
-    out = torch.empty(B, T, H, 128, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(B, T, H, dtype=torch.float32, device=dev)
-
-    def step():
-        m.plan(g.seq_lens)
-        absorb()
-        m.attend(g.cache, g.block_table, g.seq_lens, g.scale, lse)
-        m.combine(g.scale, lse)
-        up_project()
-
-    def attend_only():
-        m.attend(g.cache, g.block_table, g.seq_lens, g.scale, lse)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    st = m.check()
-    if st != 0:
-        raise SystemExit("device status %d after warm-up" % st)
-
-    # The step is launch-bound on the host for small batches: capture
-    # PER_GRAPH consecutive steps in one CUDA graph and replay it (same
-    # kernels, same arguments), so host launch overhead cannot starve the GPU.
-    per_graph = 1 if args.no_graph else min(PER_GRAPH, args.steps)
-    graph_step = graph_attend = graph_rem = None
+    r.prepare(args.warmup)
+    per_graph = r.per_call()
     rem = args.steps % per_graph
-    if not args.no_graph:
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            step()
-            attend_only()
-        stream.wait_stream(side)
+    graph_rem = None
+    if rem and r.graph_step is not None:
+        graph_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_rem):
+            for _ in range(rem):
+                r.step()
         torch.cuda.synchronize()
-        graph_step, graph_attend = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph_step):
-            for _ in range(per_graph):
-                step()
-        with torch.cuda.graph(graph_attend):
-            for _ in range(per_graph):
-                attend_only()
-        if rem:
-            graph_rem = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph_rem):
-                for _ in range(rem):
-                    step()
-        torch.cuda.synchronize()
-        for _ in range(max(1, args.warmup // per_graph)):
-            graph_step.replay()
-        torch.cuda.synchronize()
-    run_steps = graph_step.replay if graph_step is not None else step
+    run_steps = r.steps_call()
     run_rem = graph_rem.replay if graph_rem is not None else (lambda: None)
-    run_attends = graph_attend.replay if graph_attend is not None else attend_only
 
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -430,40 +522,32 @@ def main():
     if dist is not None:
         dist.barrier()
     clocks.stop()
-    st = m.check()
-    if st != 0:
-        raise SystemExit("device status %d in timed region" % st)
+    r.check("in timed region")
     elapsed = t_start.elapsed_time(t_end) / 1e3
 
-    # Average duration of the dominant kernel (attention step), CUDA events on
-    # the launching stream around back-to-back launches.
-    n_rep = max(1, min(args.steps, 2000) // per_graph)
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    for _ in range(n_rep):
-        run_attends()
-    a1.record(stream)
-    torch.cuda.synchronize()
-    attend_s = a0.elapsed_time(a1) / 1e3 / (n_rep * per_graph)
+    # Average duration of the dominant kernel (attention step): CUDA events on
+    # the launching stream around ATTEND_LAUNCHES back-to-back launches.
+    attend_s, attend_launches = r.time_attend()
+    r.check("while timing the attention step")
     elapsed = max_over_ranks(elapsed, dist, dev)
     per_step = elapsed / args.steps
 
     # ---- end to end through the same C ABI with host buffers
     host = [(getattr(inp_cpu, k).pin_memory(), getattr(g, k)) for k in
             ("q", "cache", "block_table", "seq_lens")]
-    host += [(h.pin_memory(), dv) for h, dv in wts.values()]
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    host += [(h.pin_memory(), dv) for h, dv in r.wts.values()]
+    out_h = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
+    lse_h = torch.empty(r.lse.shape, dtype=r.lse.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t, _ in host)
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
 
     def e2e_step():
         for t, dv in host:
             dv.copy_(t, non_blocking=True)
-        m.plan(g.seq_lens)
-        run_all()
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        r.plan()
+        r.run_all()
+        out_h.copy_(r.out, non_blocking=True)
+        lse_h.copy_(r.lse, non_blocking=True)
 
     n_e2e = max(3, min(args.e2e_steps, args.steps))
     for _ in range(3):
@@ -477,14 +561,14 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
+    r.check("in the end-to-end run")
     e2e_s = e0.elapsed_time(e1) / 1e3 / n_e2e
     e2e_s = max_over_ranks(e2e_s, dist, dev)
 
     breakdown = None
     if args.breakdown:
-        stages = {"plan": lambda: m.plan(g.seq_lens), "absorb": absorb,
-                  "attend": attend_only, "combine": lambda: m.combine(g.scale, lse),
-                  "up_project": up_project}
+        stages = {"plan": r.plan, "absorb": r.absorb, "attend": r.attend, "combine": r.combine,
+                  "up_project": r.up_project}
         breakdown = {}
         for name, fn in stages.items():
             gr = torch.cuda.CUDAGraph()
@@ -492,25 +576,42 @@ def main():
                 fn()
             for _ in range(5):
                 gr.replay()
-            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            b0.record(stream)
-            for _ in range(200):
-                gr.replay()
-            b1.record(stream)
-            torch.cuda.synchronize()
-            breakdown[name] = b0.elapsed_time(b1) / 200 * 1e3
-        st = m.check()
-        if st != 0:
-            raise SystemExit("device status %d in the per-stage timing" % st)
+            breakdown[name] = r.time_calls(gr.replay, 200) * 1e6
+        r.check("in the per-stage timing")
+
+    wts_host = {k: v[0] for k, v in r.wts.items()}  # the oracle leg below needs them
+
+    # ---- every full-size workload, same kernels, measured in this run
+    per_config = None
+    if not args.no_per_config:
+        per_config = {args.workload: per_config_entry(r, per_step, attend_s, attend_launches,
+                                                      hbm, bf16, peak_src)}
+        r.free()
+        cfg_clocks = ClockSampler(local)
+        cfg_clocks.start()
+        for name in PER_CONFIG:
+            if name == args.workload:
+                continue
+            rc = WorkloadRunner(name, dev, fp8, use_graph=not args.no_graph)
+            rc.prepare(args.warmup)
+            step_s = rc.time_calls(rc.steps_call(), max(1, CONFIG_STEPS // rc.per_call())) / \
+                rc.per_call()
+            a_s, a_n = rc.time_attend()
+            rc.check("in the per-config timing")
+            per_config[name] = per_config_entry(rc, step_s, a_s, a_n, hbm, bf16, peak_src)
+            rc.free()
+            torch.cuda.empty_cache()
+        cfg_clocks.stop()
+        per_config["clocks"] = cfg_clocks.summary()
 
     if rank != 0:
         dist.destroy_process_group()
         return
 
-    hbm, bf16, bf16_sus, peak_src = measured_peaks()
     gbs = world * stats["cache_bytes"] / per_step / 1e9
     tflops = world * stats["flops"] / per_step / 1e12
     roof = attention_roofline(stats, attend_s, hbm, bf16, peak_src, ncu_traffic(args.workload))
+    roof["launches_timed"] = attend_launches
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
@@ -532,19 +633,21 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3},
         "gpu_launches": args.steps * (1 + binding.lib().mla_decode_kernels_per_run()),
-        "launch_mode": ("cuda_graph, %d steps per replay" % per_graph) if graph_step is not None else "host",
+        "launch_mode": ("cuda_graph, %d steps per replay" % per_graph) if per_graph > 1 else "host",
         "clocks": clocks.summary(),
     }
     if breakdown is not None:
         line["stage_us"] = breakdown
+    if per_config is not None:
+        line["per_config"] = per_config
     if not args.no_cpu_baseline:
         import oracle
         inp_or = inp_cpu
         if fp8:  # the oracle decompresses the FP8 weights, then decodes
             import copy
             inp_or = copy.copy(inp_cpu)
-            inp_or.w_uk = oracle.dequant_fp8_weight(uk8, uk_s)
-            inp_or.w_uv = oracle.dequant_fp8_weight(uv8, uv_s)
+            inp_or.w_uk = oracle.dequant_fp8_weight(wts_host["uk8"], wts_host["uk_s"])
+            inp_or.w_uv = oracle.dequant_fp8_weight(wts_host["uv8"], wts_host["uv_s"])
         dt, nbytes, flops, tokens, text = time_oracle(inp_or, budget_s=15.0)
         line["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s",
                                 "cores": oracle.threads(), "kind": "oracle", "sample": text,

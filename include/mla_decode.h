@@ -87,7 +87,15 @@ typedef enum {
 
 /* Bytes of device workspace needed for `dims` on the current device, with the
  * default number of work ranges (one per resident decode CTA group).
- * Needs a CUDA device (queries its SM count); returns CUDA_ERROR without one. */
+ * The workspace holds the split-KV plan, the absorbed query (step 1 above),
+ * the latent output and the partial results of key ranges that the log-sum-exp
+ * merge combines ("DeepSeek publica FlashMLA como codigo abierto": FlashMLA's
+ * FlashAttention 2/3 lineage; vLLM PR #14770, PR description, for the
+ * intermediates of the sequential matmuls).  The pages give no interface; the
+ * caller-owned workspace is this library's packaging.
+ * Needs a CUDA device (queries its SM count); returns CUDA_ERROR without one.
+ * INVALID_ARG for a null `dims` or `bytes`; UNSUPPORTED for dims outside the
+ * fixed set.  No device memory is touched. */
 int mla_decode_workspace_size(const mla_decode_dims* dims, size_t* bytes);
 
 /* Same, for a plan built with `num_ranges` work ranges (0 = default).  More
@@ -99,7 +107,14 @@ int mla_decode_workspace_size_ex(const mla_decode_dims* dims, int32_t num_ranges
 /* Step a1, the planner.  Reads seq_lens (device int32 [B]) on the device and
  * writes into the workspace: the partition of all (sequence, page) work into
  * equal-cost contiguous ranges, each sequence's split count and its slots for
- * partial results.  Also clears the workspace status word.  No host sync. */
+ * partial results.  Also clears the workspace status word.  No host sync.
+ * Source: "DeepSeek publica FlashMLA como codigo abierto", feature list
+ * (FlashMLA is built for serving batches whose sequences differ in length);
+ * balancing the key ranges of such a batch over the SMs is this planner's
+ * reading of that.  Errors: INVALID_ARG (null seq_lens or workspace, workspace not
+ * 16-byte aligned), UNSUPPORTED (dims), WORKSPACE_TOO_SMALL, CUDA_ERROR
+ * (launch); seq_lens outside [q_len, max_pages_per_seq * 64] are clamped on
+ * the device and reported as DEVICE_BOUNDS by mla_decode_check. */
 int mla_decode_plan(const mla_decode_dims* dims, const int32_t* seq_lens,
                     void* workspace, size_t workspace_bytes, void* stream);
 
@@ -116,7 +131,9 @@ int mla_decode_plan_ex(const mla_decode_dims* dims, const int32_t* seq_lens,
  *               entries past ceil(L_b/64) are never read
  *   seq_lens    int32 [B]: tokens in each sequence INCLUDING its T new tokens
  *   w_uk        bf16 [H, 128, 512];  w_uv bf16 [H, 512, 128]
- *   softmax_scale: multiplies q_lat . c_j (e.g. 1/sqrt(192))
+ *   softmax_scale: multiplies q_lat . c_j (e.g. 1/sqrt(192)); must be finite
+ *               and > 0, else INVALID_ARG (the attention step takes its
+ *               running maximum over unscaled scores)
  *   out         bf16 [B, T, H, 128] (written)
  *   lse         fp32 [B, T, H] (written): natural-log log-sum-exp of the
  *               scaled scores of each query row
@@ -137,7 +154,9 @@ int mla_decode_run(const mla_decode_dims* dims, const void* q, const void* kv_ca
  *                                     the first-order correction for the bf16
  *                                     rounding of q_lat (lse is final only
  *                                     after this step)
- *   up_project: o_lat, w_uv        -> out                                   */
+ *   up_project: o_lat, w_uv        -> out
+ * attend and combine take the softmax scale and reject one that is not
+ * finite and > 0 with INVALID_ARG, as mla_decode_run does.                 */
 int mla_decode_absorb(const mla_decode_dims* dims, const void* q, const void* w_uk,
                       void* workspace, size_t workspace_bytes, void* stream);
 int mla_decode_attend(const mla_decode_dims* dims, const void* kv_cache,
@@ -176,7 +195,10 @@ int mla_decode_up_project_fp8w(const mla_decode_dims* dims, const uint8_t* w_uv_
 
 /* Waits for `stream`, then returns the first device-side status recorded in
  * the workspace since the last plan (OK, DEVICE_BOUNDS or TIMEOUT), or
- * CUDA_ERROR if the stream reports an error. */
+ * CUDA_ERROR if the stream reports an error.  INVALID_ARG for a null
+ * workspace.  The pages have no counterpart: the kernels never trap on a bad
+ * block-table entry, a bad sequence length or a wait that gave up; they record
+ * it in the workspace and this call reads it back. */
 int mla_decode_check(const void* workspace, void* stream);
 
 /* Static English text for a status code. */
@@ -199,15 +221,19 @@ int mla_decode_workspace_offsets(const mla_decode_dims* dims, int32_t num_ranges
  * forbids new allocations.  The pages describing the method have no
  * counterpart to this call; it is a packaging choice of this library.
  *
- * Arguments are those of mla_decode_run minus the workspace.  Scratch comes
+ * Arguments are those of mla_decode_run minus the workspace, checked the same
+ * way (INVALID_ARG, UNSUPPORTED) before anything is enqueued.  Scratch comes
  * from a fixed 32 MiB array in statically allocated device memory, which every
  * GPU that loads the library holds until the process exits; the call makes no
  * allocation of any kind.  If mla_decode_workspace_size(dims) exceeds 32 MiB
  * it returns MLA_DECODE_WORKSPACE_TOO_SMALL and enqueues nothing.  On a
  * 152-SM GB300 that admits up to 32 query rows per sequence (T * H <= 32, e.g.
- * 16 heads with one or two query tokens), up to roughly 130-460 sequences.  The first call on each device looks up that device's copy of the
- * array (cudaGetSymbolAddress); make that first call before any stream
- * capture.  All calls on a device share the one array, which keeps the last
+ * 16 heads with one or two query tokens), up to roughly 130-460 sequences.
+ * The first call on each device looks up that device's copy of the array
+ * (cudaGetSymbolAddress) in the device's current context; make that first
+ * call before any stream capture.  A later call in a different context of the
+ * device (after cudaDeviceReset, for example) looks the address up again, so
+ * make the first call after a reset before any capture too.  All calls on a device share the one array, which keeps the last
  * call's contents: calls whose work overlaps on the GPU (other streams, other
  * host threads) race and must be serialised by the caller.  Device-side
  * bounds errors are recorded in the shared array but cannot be queried

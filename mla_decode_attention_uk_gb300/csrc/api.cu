@@ -4,12 +4,14 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
 
 #include "../../include/mla_decode.h"
 #include "common.cuh"
+#include "host_checks.h"
 #include "ptx.cuh"
 
 namespace mla {
@@ -198,6 +200,29 @@ T* at(void* ws, size_t off) {
 
 }  // namespace
 
+namespace mla {
+
+bool softmax_scale_ok(float scale) { return std::isfinite(scale) && scale > 0.0f; }
+
+int check_run_inputs(const mla_decode_dims* d, const void* q, const void* kv_cache,
+                     const int32_t* block_table, const int32_t* seq_lens, const void* w_uk,
+                     const void* w_uv, bool fp8, const float* uk_scale, const float* uv_scale,
+                     float scale, const void* out, const float* lse) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  auto aligned4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!softmax_scale_ok(scale)) return MLA_DECODE_INVALID_ARG;
+  if (!q || !kv_cache || !block_table || !seq_lens || !w_uk || !w_uv || !out || !lse ||
+      !aligned16(q) || !aligned16(kv_cache) || !aligned16(w_uk) || !aligned16(w_uv) ||
+      !aligned16(out) || !aligned4(block_table) || !aligned4(seq_lens) || !aligned4(lse))
+    return MLA_DECODE_INVALID_ARG;
+  if (fp8 && (!uk_scale || !uv_scale || !aligned4(uk_scale) || !aligned4(uv_scale)))
+    return MLA_DECODE_INVALID_ARG;
+  return MLA_DECODE_OK;
+}
+
+}  // namespace mla
+
 extern "C" {
 
 const char* mla_decode_status_string(int s) {
@@ -348,7 +373,8 @@ int mla_decode_attend(const mla_decode_dims* d, const void* kv_cache, const int3
                       void* stream) {
   int rc = check_dims(d);
   if (rc) return rc;
-  if (!kv_cache || !block_table || !seq_lens || !lse || !ws || !aligned16(kv_cache) ||
+  if (!softmax_scale_ok(scale) || !kv_cache || !block_table || !seq_lens || !lse || !ws ||
+      !aligned16(kv_cache) ||
       !aligned16(ws) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return MLA_DECODE_INVALID_ARG;
@@ -378,7 +404,8 @@ int mla_decode_combine(const mla_decode_dims* d, float scale, float* lse, void* 
                        size_t ws_bytes, void* stream) {
   int rc = check_dims(d);
   if (rc) return rc;
-  if (!lse || !ws || !aligned16(ws) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+  if (!softmax_scale_ok(scale) || !lse || !ws || !aligned16(ws) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
     return MLA_DECODE_INVALID_ARG;
   WsLayout L;
   rc = layout_for(d, ws_bytes, &L);
@@ -411,22 +438,16 @@ int mla_decode_up_project_fp8w(const mla_decode_dims* d, const uint8_t* w_uv_fp8
 }
 
 // Every argument of a whole run, checked before its first launch so that a
-// host-detected error leaves nothing enqueued.  w_uk / w_uv are the bf16
-// weights, or with fp8 the E4M3 codes, whose block scales must then be given.
+// host-detected error leaves nothing enqueued.
 static int check_run(const mla_decode_dims* d, const void* q, const void* kv_cache,
                      const int32_t* block_table, const int32_t* seq_lens, const void* w_uk,
                      const void* w_uv, bool fp8, const float* uk_scale, const float* uv_scale,
-                     const void* out, const float* lse, const void* ws, size_t ws_bytes) {
-  int rc = check_dims(d);
+                     float scale, const void* out, const float* lse, const void* ws,
+                     size_t ws_bytes) {
+  int rc = check_run_inputs(d, q, kv_cache, block_table, seq_lens, w_uk, w_uv, fp8, uk_scale,
+                            uv_scale, scale, out, lse);
   if (rc) return rc;
-  auto aligned4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
-  if (!q || !kv_cache || !block_table || !seq_lens || !w_uk || !w_uv || !out || !lse || !ws ||
-      !aligned16(q) || !aligned16(kv_cache) || !aligned16(w_uk) || !aligned16(w_uv) ||
-      !aligned16(out) || !aligned16(ws) || !aligned4(block_table) || !aligned4(seq_lens) ||
-      !aligned4(lse))
-    return MLA_DECODE_INVALID_ARG;
-  if (fp8 && (!uk_scale || !uv_scale || !aligned4(uk_scale) || !aligned4(uv_scale)))
-    return MLA_DECODE_INVALID_ARG;
+  if (!ws || !aligned16(ws)) return MLA_DECODE_INVALID_ARG;
   WsLayout L;
   return layout_for(d, ws_bytes, &L);
 }
@@ -436,7 +457,7 @@ int mla_decode_run(const mla_decode_dims* d, const void* q, const void* kv_cache
                    const void* w_uv, float scale, void* out, float* lse, void* ws, size_t ws_bytes,
                    void* stream) {
   int rc = check_run(d, q, kv_cache, block_table, seq_lens, w_uk, w_uv, false, nullptr, nullptr,
-                     out, lse, ws, ws_bytes);
+                     scale, out, lse, ws, ws_bytes);
   if (rc) return rc;
   rc = mla_decode_absorb(d, q, w_uk, ws, ws_bytes, stream);
   if (rc) return rc;
@@ -453,7 +474,7 @@ int mla_decode_run_fp8w(const mla_decode_dims* d, const void* q, const void* kv_
                         const uint8_t* w_uv_fp8, const float* w_uv_scale, float scale, void* out,
                         float* lse, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_run(d, q, kv_cache, block_table, seq_lens, w_uk_fp8, w_uv_fp8, true, w_uk_scale,
-                     w_uv_scale, out, lse, ws, ws_bytes);
+                     w_uv_scale, scale, out, lse, ws, ws_bytes);
   if (rc) return rc;
   rc = mla_decode_absorb_fp8w(d, q, w_uk_fp8, w_uk_scale, ws, ws_bytes, stream);
   if (rc) return rc;

@@ -51,6 +51,20 @@ int main(void) {
                             p, (float*)p, p, (size_t)1 << 30, NULL) == MLA_DECODE_INVALID_ARG);
   CHECK(mla_decode_check(NULL, NULL) == MLA_DECODE_INVALID_ARG);
 
+  /* The softmax scale must be finite and > 0. */
+  const float bad_scales[3] = {0.0f, -0.07f, 1.0f / 0.0f};
+  for (int i = 0; i < 3; ++i) {
+    CHECK(mla_decode_run(&d, p, p, (const int32_t*)p, (const int32_t*)p, p, p, bad_scales[i], p,
+                         (float*)p, p, (size_t)1 << 30, NULL) == MLA_DECODE_INVALID_ARG);
+    CHECK(mla_decode_attend(&d, p, (const int32_t*)p, (const int32_t*)p, bad_scales[i], (float*)p,
+                            p, (size_t)1 << 30, NULL) == MLA_DECODE_INVALID_ARG);
+    CHECK(mla_decode_combine(&d, bad_scales[i], (float*)p, p, (size_t)1 << 30, NULL) ==
+          MLA_DECODE_INVALID_ARG);
+    CHECK(mla_decode_run_static_scratch(&d, p, p, (const int32_t*)p, (const int32_t*)p, p, p,
+                                        bad_scales[i], p, (float*)p, NULL) ==
+          MLA_DECODE_INVALID_ARG);
+  }
+
   for (int s = 0; s <= 6; ++s) CHECK(strcmp(mla_decode_status_string(s), "unknown status") != 0);
   CHECK(strcmp(mla_decode_status_string(42), "unknown status") == 0);
 

@@ -46,17 +46,3 @@ def assert_parity(stats, what=""):
     assert stats["out_max"] <= OUT_MAX, (what, stats)
     assert stats["out_mean"] <= OUT_MEAN, (what, stats)
     assert stats["lse_max"] <= LSE_MAX, (what, stats)
-
-
-def sample_rows(inp, n, seed=0, extra=()):
-    """Rows spread over the batch: first/last sequence, every head group, both query tokens."""
-    B, T, H = inp.q.shape[:3]
-    total = B * T * H
-    rng = np.random.default_rng(seed)
-    rows = set(rng.choice(total, size=min(n, total), replace=False).tolist())
-    for b in (0, B - 1):
-        for t in range(T):
-            for h in (0, H - 1):
-                rows.add((b * T + t) * H + h)
-    rows.update(extra)
-    return sorted(rows)

@@ -2,6 +2,7 @@
 every entry point declared in include/mla_decode.h, and rejects bad arguments
 before touching the device."""
 import ctypes
+import math
 import os
 import re
 
@@ -179,3 +180,55 @@ def test_workspace_layout_holds_the_documented_buffers(B, T, H, R):
     # Without a device the default range count cannot be known.
     assert L.mla_decode_workspace_size_ex(ctypes.byref(d), -1, ctypes.byref(n2)) == 1
     assert L.mla_decode_workspace_size_ex(ctypes.byref(d), 65537, ctypes.byref(n2)) == 1
+
+
+BAD_SCALES = [0.0, -0.07, float("nan"), float("inf"), -float("inf"), -0.0]
+
+
+@pytest.mark.parametrize("scale", BAD_SCALES)
+def test_softmax_scale_must_be_finite_and_positive(scale):
+    # The attention step takes its running maximum over unscaled scores, which
+    # is the maximum of the scaled ones only for a positive scale: every call
+    # that takes the scale rejects the others on the host, before any launch
+    # (without a GPU an enqueue attempt would return CUDA_ERROR instead).
+    L = binding.lib()
+    d = good_dims()
+    ok = ctypes.c_void_p(4096)
+    sc = ctypes.c_float(scale)
+    assert L.mla_decode_run(ctypes.byref(d), ok, ok, ok, ok, ok, ok, sc, ok, ok, ok,
+                            1 << 30, None) == 1
+    assert L.mla_decode_run_fp8w(ctypes.byref(d), ok, ok, ok, ok, ok, ok, ok, ok, sc, ok, ok,
+                                 ok, 1 << 30, None) == 1
+    assert L.mla_decode_attend(ctypes.byref(d), ok, ok, ok, sc, ok, ok, 1 << 30, None) == 1
+    assert L.mla_decode_combine(ctypes.byref(d), sc, ok, ok, 1 << 30, None) == 1
+    assert L.mla_decode_run_static_scratch(ctypes.byref(d), ok, ok, ok, ok, ok, ok, sc, ok, ok,
+                                           None) == 1
+
+
+def test_smallest_positive_scale_passes_the_check():
+    # A tiny but positive, finite scale is valid: the call gets past the
+    # argument check (and, without a GPU, fails only when it reaches the device).
+    L = binding.lib()
+    d = good_dims()
+    ok = ctypes.c_void_p(4096)
+    sc = ctypes.c_float(math.ldexp(1.0, -149))
+    assert L.mla_decode_combine(ctypes.byref(d), sc, ok, ok, 64, None) == 3
+
+
+def test_static_scratch_checks_every_argument_before_anything_else():
+    # The workspace-free call rejects bad arguments before it sizes its scratch
+    # or enqueues the planner on the shared array.  Without a GPU, sizing would
+    # return CUDA_ERROR (4): INVALID_ARG / UNSUPPORTED show the check ran first.
+    L = binding.lib()
+    d = good_dims()
+    ok, bad = ctypes.c_void_p(4096), ctypes.c_void_p(4096 + 2)
+    sc = ctypes.c_float(0.07)
+    args = [ok, ok, ok, ok, ok, ok, sc, ok, ok]
+    for i, v in ((0, None), (0, bad), (1, bad), (2, ctypes.c_void_p(4097)), (3, None),
+                 (4, bad), (5, None), (7, bad), (8, ctypes.c_void_p(4098))):
+        a = list(args)
+        a[i] = v
+        assert L.mla_decode_run_static_scratch(ctypes.byref(d), *a, None) == 1, i
+    bad_dims = good_dims(kv_lora=256)
+    assert L.mla_decode_run_static_scratch(ctypes.byref(bad_dims), *args, None) == 2
+    assert L.mla_decode_run_static_scratch(None, *args, None) == 1

@@ -206,8 +206,8 @@ def test_unreferenced_nan_pages_are_never_read():
 def test_split_and_lse_combine_equal_unsplit(k):
     L = 203
     inp = rand_case(17, 1, [L], 1, 2)
-    _, lse, olat = oracle.decode(inp.q, inp.cache, inp.block_table, inp.seq_lens, inp.w_uk,
-                                 inp.w_uv, inp.scale, want_olat=True)
+    out, lse, olat = oracle.decode(inp.q, inp.cache, inp.block_table, inp.seq_lens, inp.w_uk,
+                                   inp.w_uv, inp.scale, want_olat=True)
     r = random.Random(k)
     cuts = sorted(r.sample(range(1, L), k - 1))  # ranges end mid-page in general
     bounds = [0] + cuts + [L]
@@ -217,8 +217,33 @@ def test_split_and_lse_combine_equal_unsplit(k):
         lse_c, o_c = oracle.combine([p[1] for p in parts], np.stack([p[0] for p in parts]))
         assert lse_c == pytest.approx(lse[h], rel=1e-13, abs=1e-13)
         np.testing.assert_allclose(o_c, olat[h], rtol=1e-12, atol=1e-14)
+        # the merged latent output, mapped back by W_UV, is the unsplit out
         up = oracle.up_project(inp.w_uv, h, o_c)
-        assert up.shape == (128,)
+        np.testing.assert_allclose(up, out[h], rtol=1e-11, atol=1e-13)
+
+
+def _up_project_rows(up_fn, inp, olat):
+    B, T, H = inp.q.shape[:3]
+    return np.stack([up_fn(inp.w_uv, r % H, olat[r]) for r in range(B * T * H)])
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_up_project_matches_explicit_value_projection(seed):
+    """mla_oracle_up_project (o_lat . W_UV[h]) against the non-absorbed form,
+    which decompresses V_h = C_lat W_UV[h] first and then takes the softmax
+    average of V_h's rows: the other association of the same product (vLLM PR
+    #14770, PR description).  Each row must use its own head's W_UV."""
+    r = random.Random(100 + seed)
+    T = r.choice([1, 2])
+    B, H = r.randint(1, 3), 3
+    lens = [r.randint(T, 200) for _ in range(B)]
+    inp = rand_case(300 + seed, B, lens, T, H)
+    out, _, olat = oracle.decode(inp.q, inp.cache, inp.block_table, inp.seq_lens, inp.w_uk,
+                                 inp.w_uv, inp.scale, want_olat=True)
+    up = _up_project_rows(oracle.up_project, inp, olat)
+    eo, _ = explicit_numpy(inp)
+    np.testing.assert_allclose(up, eo, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(up, out, rtol=1e-12, atol=1e-14)
 
 
 def test_causal_pair_first_query_equals_single_query_on_shorter_sequence():
@@ -388,6 +413,49 @@ def test_planted_mistake_fails_a_pin(name, mutant_dir):
     caught = rc != 0 or not (np.allclose(out, eo, rtol=1e-9, atol=1e-11)
                              and np.allclose(lse, el, rtol=1e-11, atol=1e-11))
     assert caught, "planted mistake %s went unnoticed" % name
+
+
+UP_PROJECT_MUTANTS = {
+    "up_project_w_uv_transposed": ("acc += o_lat[l] * bf16_to_double(wv[(int64_t)l * dv + v]);",
+                                   "acc += o_lat[l] * bf16_to_double(wv[(int64_t)v * dl + l]);"),
+    "up_project_last_latent_dropped": ("for (int l = 0; l < dl; ++l) acc += o_lat[l]",
+                                       "for (int l = 0; l < dl - 1; ++l) acc += o_lat[l]"),
+    "up_project_head_ignored": ("const uint16_t* wv = w_uv + (int64_t)h * dl * dv;\n  for (int v = 0; v < dv; ++v) {\n    double acc = 0.0;\n    for (int l = 0; l < dl; ++l) acc += o_lat[l]",
+                                "const uint16_t* wv = w_uv;\n  for (int v = 0; v < dv; ++v) {\n    double acc = 0.0;\n    for (int l = 0; l < dl; ++l) acc += o_lat[l]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(UP_PROJECT_MUTANTS))
+def test_planted_mistake_in_up_project_fails_its_pin(name, mutant_dir):
+    """A mistake planted in mla_oracle_up_project must break the explicit-form pin."""
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "mla_oracle.c")).read()
+    old, new = UP_PROJECT_MUTANTS[name]
+    assert src.count(old) == 1, name
+    d = mutant_dir / name
+    d.mkdir()
+    (d / "mla_oracle.c").write_text(src.replace(old, new))
+    shutil.copy(os.path.join(os.path.dirname(oracle.__file__), "mla_oracle.h"), d / "mla_oracle.h")
+    so = d / "libm.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-o", str(so),
+                    str(d / "mla_oracle.c"), "-lm"], check=True)
+    L = ctypes.CDLL(str(so))
+    L.mla_oracle_up_project.argtypes = oracle.lib().mla_oracle_up_project.argtypes
+
+    def mutated_up(w_uv, h, o_lat):
+        H, lora, v = w_uv.shape
+        dm = oracle.Dims(1, 1, H, 0, 0, lora, v, 1, 1, 1)
+        ol = np.ascontiguousarray(o_lat, dtype=np.float64)
+        res = np.empty((v,))
+        assert L.mla_oracle_up_project(ctypes.byref(dm), w_uv.contiguous().view(torch.int16).data_ptr(),
+                                       h, ol.ctypes.data, res.ctypes.data) == 0
+        return res
+
+    inp = rand_case(22, 2, [70, 129], 2, 3)
+    _, _, olat = oracle.decode(inp.q, inp.cache, inp.block_table, inp.seq_lens, inp.w_uk,
+                               inp.w_uv, inp.scale, want_olat=True)
+    up = _up_project_rows(mutated_up, inp, olat)
+    eo, _ = explicit_numpy(inp)
+    assert not np.allclose(up, eo, rtol=1e-9, atol=1e-11), "planted mistake %s went unnoticed" % name
 
 
 # ---------------------------------------------------------------------------
