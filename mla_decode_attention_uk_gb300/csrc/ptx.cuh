@@ -44,17 +44,22 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-// Polls phase `parity` of an mbarrier once (try_wait: the thread may be
-// suspended for a system-chosen time while the phase is incomplete; measured
-// ahead of test_wait and of a 64 ns suspend hint).
+// Polls phase `parity` of an mbarrier once.  try_wait may suspend the thread
+// while the phase is incomplete; the suspend-time hint caps that at
+// kWaitHintNs.  Measured on the attention kernel, whose page pipeline is a
+// chain of hand-offs between warps: with any explicit hint from 10 to 200 ns
+// the waiting warps resume sooner than with the system-chosen limit (attention
+// 4 % faster on the 128-head batches, unchanged on 16 heads), while a
+// non-suspending test_wait spin steals issue slots from the softmax warps.
+constexpr uint32_t kWaitHintNs = 20;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "n"(kWaitHintNs)
       : "memory");
   return ok != 0;
 }
