@@ -42,6 +42,30 @@ def test_absorb_bmm_matches_fp32_matmul():
     assert (hi[:, :512].double() - ref).abs().max().item() <= ref.abs().max().item() * 2 ** -8
 
 
+@pytest.mark.parametrize("B,T,H", [(200, 2, 16), (130, 2, 128), (256, 1, 32)])
+def test_absorb_bmm_large_token_counts_matches_fp64(B, T, H):
+    # 128-token tiles: 400 and 260 tokens leave a ragged last tile, 256 is two
+    # full ones; 16, 32 and 128 heads.  Same bound as the small case above.
+    g = torch.Generator().manual_seed(40 + B + H)
+    lens = torch.randint(T, 200, (B,), generator=g).tolist()
+    inp = make_inputs(B, lens, T, H, seed=42 + H)
+    dev = torch.device("cuda")
+    gd = inp.to(dev)
+    m = binding.MlaDecode(binding.dims_for(gd.q, gd.cache, gd.block_table), dev)
+    m.absorb(gd.q, gd.w_uk)
+    torch.cuda.synchronize()
+    hi = m.q_lat().float().cpu()
+    lo = m.q_lo().float().cpu()
+    ref = torch.einsum("bthk,hkl->bthl", inp.q[..., :128].double(), inp.w_uk.double())
+    ref = ref.reshape(-1, 512)
+    got = hi[:, :512].double() + lo.double()
+    assert ((got - ref).abs() <= ref.abs() * 2.0 ** -16 + 2e-6).all()
+    assert torch.equal(hi[:, 512:], inp.q[..., 128:].reshape(-1, 64).float())
+    assert (hi[:, :512].double() - ref).abs().max().item() <= ref.abs().max().item() * 2 ** -8
+    out, lse, _ = run_gpu(inp)
+    assert_parity(compare(inp, out, lse), "absorb B=%d T=%d H=%d" % (B, T, H))
+
+
 def test_tiny_workload_all_rows():
     inp = workload_inputs("tiny")
     out, lse, _ = run_gpu(inp)
