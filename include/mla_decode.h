@@ -145,7 +145,8 @@ int mla_decode_run(const mla_decode_dims* dims, const void* q, const void* kv_ca
 
 /* The four steps of mla_decode_run as separate calls, in this order, on one
  * workspace after mla_decode_plan (for profiling one step at a time).
- *   absorb:     q, w_uk            -> q_lat (bf16 hi and lo parts, workspace)
+ *   absorb:     q, w_uk            -> q_lat (bf16 part, and the residual q_lo
+ *                                     as E4M3 of q_lo * 2^10, workspace)
  *   attend:     q_lat, cache, ...  -> o_lat + lse (from the bf16 part of q_lat)
  *                                     for unsplit sequences, fp32 partials for
  *                                     split ones
@@ -207,7 +208,8 @@ const char* mla_decode_status_string(int status);
 /* Introspection for tests and profiling: byte offsets inside a workspace
  * planned with `num_ranges` (0 = default) of the intermediate buffers
  *   offsets[0] q_lat  bf16 [B*T*H, 576]   (absorbed query, bf16 part)
- *   offsets[1] q_lo   bf16 [B*T*H, 512]   (residual q_lat - bf16 part)
+ *   offsets[1] q_lo   uint8 [B*T*H, 512]  (residual q_lat - bf16 part, times
+ *                                          2^10, as FP8 E4M3 codes)
  *   offsets[2] o_lat  bf16 [B*T*H, 512]   (latent attention output)
  *   offsets[3] plan header (int32 num_ranges, per, total_cost, num_slots)
  * n must be >= 4.  Not needed for normal use. */

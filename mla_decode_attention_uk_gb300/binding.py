@@ -183,14 +183,15 @@ class MlaDecode:
     def _view(self, key, cols, dtype=torch.bfloat16):
         off = workspace_offsets(self.dims, self.num_ranges)[key]
         rows = self.dims.batch * self.dims.q_len * self.dims.num_heads
-        n = rows * cols * 2
+        n = rows * cols * torch.empty(0, dtype=dtype).element_size()
         return self.workspace[off:off + n].view(dtype).view(rows, cols)
 
     def q_lat(self):
         return self._view("qlat", 576)
 
     def q_lo(self):
-        return self._view("qlo", 512)
+        """The residual q_lat - bf16(q_lat), times 2^10, as raw E4M3 bytes."""
+        return self._view("qlo", 512, torch.uint8)
 
     def o_lat(self):
         return self._view("olat", 512)

@@ -21,7 +21,7 @@ cudaError_t launch_plan(const int32_t* seq_lens, int B, int T, int max_pages, in
                         int32_t* seq_len_eff, int32_t* prefix, cudaStream_t stream);
 int bmm_token_tile(int BT, bool absorb);
 cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q, int BT, int H,
-                          const __nv_bfloat16* q, __nv_bfloat16* qlat, __nv_bfloat16* qlo,
+                          const __nv_bfloat16* q, __nv_bfloat16* qlat, uint8_t* qlo,
                           int32_t* status, cudaStream_t st, const uint8_t* wuk8,
                           const float* wuk_scale);
 cudaError_t launch_up_project(const CUtensorMap& tm_wuv, const CUtensorMap& tm_olat, int BT,
@@ -34,11 +34,11 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
                           const int32_t* block_table, const int32_t* seq_len_eff,
                           const PlanHeader* header, void* ws, const int32_t* seq_first,
                           const int32_t* seq_nsplit, const int32_t* seq_slot,
-                          const __nv_bfloat16* qlo, __nv_bfloat16* olat, float* lse,
+                          __nv_bfloat16* olat, float* lse,
                           int32_t* status, int B, int T, int H, int max_pages,
                           int num_pages, float scale, cudaStream_t st);
 cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, const void* ws,
-                           const PlanHeader* header, const __nv_bfloat16* qlo,
+                           const PlanHeader* header, const uint8_t* qlo,
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
                            int splits_per_seq, cudaStream_t st);
 }  // namespace mla
@@ -319,7 +319,7 @@ static int absorb_impl(const mla_decode_dims* d, const void* q, const void* w_uk
                       false)))
     return MLA_DECODE_CUDA_ERROR;
   return cuda_rc(launch_absorb(tm_w, tm_q, BT, H, static_cast<const __nv_bfloat16*>(q),
-                               at<__nv_bfloat16>(ws, L.qlat), at<__nv_bfloat16>(ws, L.qlo),
+                               at<__nv_bfloat16>(ws, L.qlat), at<uint8_t>(ws, L.qlo),
                                at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream), w8,
                                w8_scale));
 }
@@ -395,7 +395,7 @@ int mla_decode_attend(const mla_decode_dims* d, const void* kv_cache, const int3
   return cuda_rc(launch_decode(
       tm_q, tm_c, groups, block_table, at<int32_t>(ws, L.seq_len_eff), at<PlanHeader>(ws, L.header),
       ws, at<int32_t>(ws, L.seq_first), at<int32_t>(ws, L.seq_nsplit), at<int32_t>(ws, L.seq_slot),
-      at<__nv_bfloat16>(ws, L.qlo), at<__nv_bfloat16>(ws, L.olat), lse,
+      at<__nv_bfloat16>(ws, L.olat), lse,
       at<int32_t>(ws, L.status), d->batch, d->q_len, d->num_heads, d->max_pages_per_seq,
       d->num_pages, scale, static_cast<cudaStream_t>(stream)));
 }
@@ -418,7 +418,7 @@ int mla_decode_combine(const mla_decode_dims* d, float scale, float* lse, void* 
   if (rc) return rc;
   const int splits_per_seq = ranges < d->batch ? 1 : (ranges + d->batch - 1) / d->batch;
   return cuda_rc(launch_combine(at<int32_t>(ws, L.seq_nsplit), at<int32_t>(ws, L.seq_slot), ws,
-                                at<PlanHeader>(ws, L.header), at<__nv_bfloat16>(ws, L.qlo),
+                                at<PlanHeader>(ws, L.header), at<uint8_t>(ws, L.qlo),
                                 at<__nv_bfloat16>(ws, L.olat), lse, d->batch, d->q_len,
                                 d->num_heads, scale, splits_per_seq,
                                 static_cast<cudaStream_t>(stream)));

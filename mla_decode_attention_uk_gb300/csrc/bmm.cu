@@ -16,8 +16,9 @@
 // MMAs, warp 2 owns TMEM; warps 0-3 move the accumulator out of TMEM and all
 // warps store the tile.
 //
-// The absorb epilogue also writes the bf16 residual q_lat - bf16(q_lat), which
-// the attention step uses to correct its log-sum-exp to first order; the
+// The absorb epilogue also writes the residual q_lat - bf16(q_lat), scaled by
+// 2^10 and stored as FP8 E4M3, which the combine step uses to correct the
+// log-sum-exp to first order; the
 // q_pe columns of q_lat are copied by the warps not busy with TMA or MMAs
 // while the MMAs run.
 //
@@ -101,7 +102,7 @@ template <BmmMode MODE, int NT, int STAGES, bool W8>
 __global__ void __launch_bounds__(W8 ? kBmmThreadsW8 : kBmmThreads)
 bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
            int BT, int H, int K, int Kx, const __nv_bfloat16* __restrict__ q,
-           __nv_bfloat16* __restrict__ out_hi, __nv_bfloat16* __restrict__ out_lo,
+           __nv_bfloat16* __restrict__ out_hi, uint8_t* __restrict__ out_lo,
            int32_t* __restrict__ status, Fp8Weights w8) {
   constexpr int RAWS = raw_tiles(MODE, W8);
   constexpr int kRing = RAWS > 0 ? RAWS : 1;  // ring length as a divisor
@@ -326,13 +327,14 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
 
   // Epilogue.  Thread (warp w < 4, lane i) owns feature m0 + 32 w + i: it
   // moves its accumulator column (one value per token) into a bf16
-  // [token][128 m] tile in the now idle pipeline smem, then all threads copy
-  // whole 256-byte token rows to global memory with 16-byte stores.
+  // [token][128 m] tile in the now idle pipeline smem (and, absorbing, the
+  // E4M3 residual into a byte tile), then all threads copy whole token rows
+  // (256 + 128 bytes) to global memory with 16-byte stores.
   const bool have = mbar_wait(smem_u32(&done_bar), 0, &abort_sh, status);
   tc_fence_after();
   const int ml = warp * 32 + lane;
   __nv_bfloat16* const tile_hi = reinterpret_cast<__nv_bfloat16*>(sbase_ptr);
-  __nv_bfloat16* const tile_lo = tile_hi + NT * 128;
+  uint8_t* const tile_lo = reinterpret_cast<uint8_t*>(tile_hi + NT * 128);
   const bool go = have && !abort_sh;
   if (go && warp < 4) {  // a warp reaches TMEM lanes 32 (warp % 4) .. + 31
     constexpr int kCols = NT >= 32 ? 32 : 16;  // tokens per TMEM load
@@ -351,7 +353,8 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
         const __nv_bfloat16 hv = __float2bfloat16_rn(v);
         tile_hi[(c0 + j) * 128 + ml] = hv;
         if constexpr (MODE == BmmMode::kAbsorb)
-          tile_lo[(c0 + j) * 128 + ml] = __float2bfloat16_rn(v - __bfloat162float(hv));
+          tile_lo[(c0 + j) * 128 + ml] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(
+              (v - __bfloat162float(hv)) * kQloScale, __NV_SATFINITE, __NV_E4M3));
       }
     }
   }
@@ -363,12 +366,18 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
       const int tl = i >> 4, ch = i & 15;
       const size_t row = static_cast<size_t>(tok0 + tl) * H + h;
       const uint4 vh = *reinterpret_cast<const uint4*>(tile_hi + tl * 128 + ch * 8);
-      if constexpr (MODE == BmmMode::kAbsorb) {
+      if constexpr (MODE == BmmMode::kAbsorb)
         *reinterpret_cast<uint4*>(out_hi + row * kDqk + m0 + ch * 8) = vh;
-        const uint4 vl = *reinterpret_cast<const uint4*>(tile_lo + tl * 128 + ch * 8);
-        *reinterpret_cast<uint4*>(out_lo + row * kLora + m0 + ch * 8) = vl;
-      } else {
+      else
         *reinterpret_cast<uint4*>(out_hi + row * kVHead + m0 + ch * 8) = vh;
+    }
+    if constexpr (MODE == BmmMode::kAbsorb) {
+      // 8 chunks of 16 B (128 E4M3 residuals) per token row.
+      for (int i = threadIdx.x; i < ntok * 8; i += kThreads) {
+        const int tl = i >> 3, ch = i & 7;
+        const size_t row = static_cast<size_t>(tok0 + tl) * H + h;
+        *reinterpret_cast<uint4*>(out_lo + row * kLora + m0 + ch * 16) =
+            *reinterpret_cast<const uint4*>(tile_lo + tl * 128 + ch * 16);
       }
     }
   }
@@ -384,7 +393,7 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
 template <BmmMode MODE, int NT, int kStagesAll = 0>
 cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, int H, int K,
                           int Kx, int Mtot, const __nv_bfloat16* q, __nv_bfloat16* hi,
-                          __nv_bfloat16* lo, int32_t* status, cudaStream_t st,
+                          uint8_t* lo, int32_t* status, cudaStream_t st,
                           Fp8Weights w8) {
   // Two stages for the absorb step (K = 128) and for 128-token tiles (64 KB of
   // stages, three CTAs per SM); four for the up-projection's smaller tiles,
@@ -419,7 +428,7 @@ int bmm_token_tile(int BT, bool absorb) {
 }
 
 cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q, int BT, int H,
-                          const __nv_bfloat16* q, __nv_bfloat16* qlat, __nv_bfloat16* qlo,
+                          const __nv_bfloat16* q, __nv_bfloat16* qlat, uint8_t* qlo,
                           int32_t* status, cudaStream_t st, const uint8_t* wuk8,
                           const float* wuk_scale) {
   const Fp8Weights w8{wuk8, wuk_scale, kLora};

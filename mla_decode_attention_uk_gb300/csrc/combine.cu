@@ -12,7 +12,8 @@
 // scale * (q_lo . o): the attention step scored keys with the bf16 part of the
 // absorbed query, q_lat = hi + q_lo, and d lse / d q_lat = scale * o, so adding
 // scale * (q_lo . o) restores the scores of the full-precision query up to
-// second order in q_lo (|q_lo| <= 2^-9 |q_lat|).
+// second order in q_lo (|q_lo| <= 2^-9 |q_lat|).  q_lo arrives as E4M3 of
+// q_lo * 2^10 (the correction needs far less precision than the scores).
 // One warp per query row; each lane owns 16 of the 512 latent columns and
 // moves them with 16-byte vector loads.  Three instantiations:
 //   - split loop not unrolled, when most rows are unsplit (64 registers, four
@@ -23,6 +24,8 @@
 //     split's partial output together with its lse (one memory round trip
 //     instead of two), when sequences are cut into a few splits.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -33,13 +36,22 @@ namespace mla {
 namespace {
 
 constexpr int kCombThreads = 256;
+
+// Two E4M3 values (the low 16 bits of `bits`, first value in the low byte) of
+// the scaled residual q_lo * 2^10, widened exactly to fp32.
+__device__ __forceinline__ float2 qlo_pair(uint32_t bits) {
+  const __nv_fp8x2_storage_t pr = static_cast<__nv_fp8x2_storage_t>(bits & 0xFFFFu);
+  return __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
+}
 constexpr int kRowsPerCta = kCombThreads / 32;
 
+// At least three CTAs per SM: the unrolled instantiations then get up to 85
+// registers and do not spill (left to itself ptxas picks 64 and spills).
 template <int kUnroll, bool kFew>
-__global__ void __launch_bounds__(kCombThreads)
+__global__ void __launch_bounds__(kCombThreads, 3)
 combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict__ seq_slot,
                const uint8_t* __restrict__ ws, const PlanHeader* __restrict__ header, int B,
-               int T, int H, const __nv_bfloat16* __restrict__ qlo,
+               int T, int H, const uint8_t* __restrict__ qlo,
                __nv_bfloat16* __restrict__ olat, float* __restrict__ lse_out, float scale) {
   // The plan and q_lo are complete when this kernel starts (the attention
   // step waited for them before letting it launch), so they are read before
@@ -58,34 +70,34 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
   if (ns <= 1) {
     // Unsplit: o_lat and lse were written by the attention step.
     const uint4* o4 = reinterpret_cast<const uint4*>(olat + row * kLora) + lane * 2;
-    const uint4* l4 = reinterpret_cast<const uint4*>(qlo + row * kLora) + lane * 2;
-    const uint4 lv0 = l4[0], lv1 = l4[1];
+    // This lane's 16 latent columns of q_lo: 16 E4M3 bytes.
+    const uint4 lv = *(reinterpret_cast<const uint4*>(qlo + row * kLora) + lane);
     griddep_wait();
     // The row's lse goes out with the o_lat loads: one round trip, not two.
     const float lse_in = lane == 0 ? lse_out[row] : 0.0f;
     float corr = 0.0f;
+    const uint32_t lw[4] = {lv.x, lv.y, lv.z, lv.w};
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const uint4 ov = o4[q], lv = q == 0 ? lv0 : lv1;
+      const uint4 ov = o4[q];
       const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
-      const uint32_t lw[4] = {lv.x, lv.y, lv.z, lv.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(&ow[e]);
-        const __nv_bfloat162 l2 = *reinterpret_cast<const __nv_bfloat162*>(&lw[e]);
-        corr += __low2float(l2) * __low2float(o2) + __high2float(l2) * __high2float(o2);
+        const float2 l2 = qlo_pair(lw[2 * q + (e >> 1)] >> (16 * (e & 1)));
+        corr += l2.x * __low2float(o2) + l2.y * __high2float(o2);
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) corr += __shfl_xor_sync(0xffffffffu, corr, o);
-    if (lane == 0) lse_out[row] = lse_in + scale * corr;
+    if (lane == 0) lse_out[row] = lse_in + scale * kQloInvScale * corr;
     return;
   }
   const int slot0 = seq_slot[b];
-  uint2 lo_raw[4];
+  uint32_t lo_raw[4];  // 4 E4M3 residuals per (q, lane): columns (32 q + lane) * 4 ..
 #pragma unroll
   for (int q = 0; q < 4; ++q)
-    lo_raw[q] = *reinterpret_cast<const uint2*>(qlo + row * kLora + (q * 32 + lane) * 4);
+    lo_raw[q] = *reinterpret_cast<const uint32_t*>(qlo + row * kLora + (q * 32 + lane) * 4);
   griddep_wait();
   const WsLayout L = make_layout(B, T, H, header->num_ranges);
   const float* __restrict__ opart = reinterpret_cast<const float*>(ws + L.opart);
@@ -174,10 +186,9 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int col = (q * 32 + lane) * 4;
-    const __nv_bfloat162 l01 = *reinterpret_cast<const __nv_bfloat162*>(&lo_raw[q].x);
-    const __nv_bfloat162 l23 = *reinterpret_cast<const __nv_bfloat162*>(&lo_raw[q].y);
-    corr += __low2float(l01) * acc[q].x + __high2float(l01) * acc[q].y +
-            __low2float(l23) * acc[q].z + __high2float(l23) * acc[q].w;
+    const float2 l01 = qlo_pair(lo_raw[q]);
+    const float2 l23 = qlo_pair(lo_raw[q] >> 16);
+    corr += l01.x * acc[q].x + l01.y * acc[q].y + l23.x * acc[q].z + l23.y * acc[q].w;
     __nv_bfloat162 o01 = __floats2bfloat162_rn(acc[q].x, acc[q].y);
     __nv_bfloat162 o23 = __floats2bfloat162_rn(acc[q].z, acc[q].w);
     uint2 packed;
@@ -187,13 +198,13 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) corr += __shfl_xor_sync(0xffffffffu, corr, o);
-  if (lane == 0) lse_out[row] = lse + scale * corr;
+  if (lane == 0) lse_out[row] = lse + scale * kQloInvScale * corr;
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, const void* ws,
-                           const PlanHeader* header, const __nv_bfloat16* qlo,
+                           const PlanHeader* header, const uint8_t* qlo,
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
                            int splits_per_seq, cudaStream_t st) {
   dim3 grid((T * H + kRowsPerCta - 1) / kRowsPerCta, B);

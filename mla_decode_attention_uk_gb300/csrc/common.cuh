@@ -45,6 +45,15 @@ constexpr int kBoxes = kDqk / kBoxCols;        // 9 column boxes per 576-wide ro
 constexpr int kLatBoxes = kLora / kBoxCols;    // 8 of them hold latent columns
 constexpr int kBoxBytes = 64 * 128;            // 64 rows x 128 B
 
+// The residual of the absorbed query, q_lo = q_lat - bf16(q_lat), feeds only
+// the first-order LSE correction scale * (q_lo . o_lat).  It is stored as FP8
+// E4M3 of q_lo * 2^kQloShift (|q_lo| <= 2^-9 |q_lat|, so the scaled values of
+// |q_lat| up to about 200 stay below E4M3's largest finite 448): half the bytes
+// of bf16, at a cost of about 1e-4 in the LSE (the tolerance is 1e-3).
+constexpr int kQloShift = 10;
+constexpr float kQloScale = 1024.0f;          // 2^kQloShift
+constexpr float kQloInvScale = 1.0f / 1024.0f;
+
 // Cost of starting a piece of work (loading Q, writing the result), in pages.
 constexpr int kPieceCost = 2;
 
@@ -81,7 +90,7 @@ struct WsLayout {
   size_t seq_len_eff; // int32 [B]  lengths clamped to [T, max_pages*64]
   size_t prefix;      // int32 [B+1] exclusive prefix of per-sequence cost
   size_t qlat;        // bf16 [B*T*H, 576]  absorbed query, bf16 part
-  size_t qlo;         // bf16 [B*T*H, 512]  absorbed query, residual (q_lat - bf16 part)
+  size_t qlo;         // E4M3 [B*T*H, 512]  absorbed query residual (q_lat - bf16 part) * 2^10
   size_t olat;        // bf16 [B*T*H, 512]  latent attention output
   size_t range_b;     // int32 [R+1]                     (R-dependent from here on)
   size_t range_p;     // int32 [R+1]
@@ -108,7 +117,7 @@ __host__ __device__ inline WsLayout make_layout(int B, int T, int H, int R) {
   L.seq_len_eff = take(sizeof(int32_t) * B);
   L.prefix = take(sizeof(int32_t) * (B + 1));
   L.qlat = take(rows * kDqk * 2);
-  L.qlo = take(rows * kLora * 2);
+  L.qlo = take(rows * kLora);
   L.olat = take(rows * kLora * 2);
   L.range_b = take(sizeof(int32_t) * (R + 1));
   L.range_p = take(sizeof(int32_t) * (R + 1));

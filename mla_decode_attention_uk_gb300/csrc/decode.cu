@@ -82,7 +82,6 @@ struct DecodeParams {
   const int32_t* seq_first;
   const int32_t* seq_nsplit;
   const int32_t* seq_slot;
-  const __nv_bfloat16* qlo;  // [B*T*H, 512]
   __nv_bfloat16* olat;       // [B*T*H, 512]
   float* lse;                // [B*T*H]
   float* opart;              // [slots, T*H, 512]
@@ -650,7 +649,7 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
                           const int32_t* block_table, const int32_t* seq_len_eff,
                           const PlanHeader* header, void* ws, const int32_t* seq_first,
                           const int32_t* seq_nsplit, const int32_t* seq_slot,
-                          const __nv_bfloat16* qlo, __nv_bfloat16* olat, float* lse,
+                          __nv_bfloat16* olat, float* lse,
                           int32_t* status, int B, int T, int H, int max_pages,
                           int num_pages, float scale, cudaStream_t st) {
   const int smem = decode_smem_bytes(T, H);
@@ -667,7 +666,6 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
   P.seq_first = seq_first;
   P.seq_nsplit = seq_nsplit;
   P.seq_slot = seq_slot;
-  P.qlo = qlo;
   P.olat = olat;
   P.lse = lse;
   P.opart = nullptr;

@@ -153,7 +153,8 @@ def test_fp8_step_calls_check_their_scales():
                                      (64, 8, 128, 9), (5000, 1, 16, 152), (1, 1, 48, 1)])
 def test_workspace_layout_holds_the_documented_buffers(B, T, H, R):
     # With an explicit range count the sizing needs no device.  The header
-    # documents q_lat bf16 [B*T*H, 576], q_lo and o_lat bf16 [B*T*H, 512];
+    # documents q_lat bf16 [B*T*H, 576], q_lo E4M3 bytes [B*T*H, 512] and
+    # o_lat bf16 [B*T*H, 512];
     # the split partials (two slots per range: fp32 lse [T*H] and o [T*H, 512]
     # each) come after them.
     L = binding.lib()
@@ -167,7 +168,7 @@ def test_workspace_layout_holds_the_documented_buffers(B, T, H, R):
     assert all(o % 16 == 0 for o in off)
     assert header + 16 <= q_lat  # plan header (four int32) before the buffers
     assert q_lat + rows * 576 * 2 <= q_lo
-    assert q_lo + rows * 512 * 2 <= o_lat
+    assert q_lo + rows * 512 <= o_lat
     partials = 2 * R * T * H * (512 + 1) * 4
     assert o_lat + rows * 512 * 2 + partials <= n.value
     # Each extra range adds two partial slots (and its range bounds): at least

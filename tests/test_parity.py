@@ -20,6 +20,12 @@ from parity_util import assert_parity, compare, run_gpu
 pytestmark = pytest.mark.gpu
 
 
+def q_lo_values(m):
+    """The residual the absorb step stores (E4M3 codes of q_lo * 2^10), decoded
+    with PyTorch's float8_e4m3fn."""
+    return m.q_lo().cpu().view(torch.float8_e4m3fn).float() * 2.0 ** -10
+
+
 def test_absorb_bmm_matches_fp32_matmul():
     inp = make_inputs(3, [70, 5, 300], 2, 32, seed=41)
     dev = torch.device("cuda")
@@ -29,16 +35,17 @@ def test_absorb_bmm_matches_fp32_matmul():
     m.absorb(g.q, g.w_uk)
     torch.cuda.synchronize()
     hi = m.q_lat().float().cpu()
-    lo = m.q_lo().float().cpu()
+    lo = q_lo_values(m)
     ref = torch.einsum("bthk,hkl->bthl", inp.q[..., :128].double(), inp.w_uk.double())
     ref = ref.reshape(-1, 512)
     got = hi[:, :512].double() + lo.double()
-    # hi + lo carries ~16 significant bits: the bf16 rounding of the residual
-    # is at most 2^-9 of a residual that is itself at most 2^-9 of the value;
-    # fp32 accumulation over K = 128 adds far less.
-    assert ((got - ref).abs() <= ref.abs() * 2.0 ** -16 + 2e-6).all()
+    # hi + lo carries ~13 significant bits: the E4M3 rounding of the residual
+    # is at most 2^-4 of a residual that is itself at most 2^-9 of the value
+    # (plus E4M3's subnormal step 2^-9 at the 2^10 scale); fp32 accumulation
+    # over K = 128 adds far less.
+    assert ((got - ref).abs() <= ref.abs() * 2.0 ** -13 + 2.0 ** -19 + 2e-6).all()
     assert torch.equal(hi[:, 512:], inp.q[..., 128:].reshape(-1, 64).float())
-    # hi is the bf16 rounding of the fp32 product, lo the bf16 rounding of the rest
+    # hi is the bf16 rounding of the fp32 product, lo the E4M3 rounding of the rest
     assert (hi[:, :512].double() - ref).abs().max().item() <= ref.abs().max().item() * 2 ** -8
 
 
@@ -55,11 +62,11 @@ def test_absorb_bmm_large_token_counts_matches_fp64(B, T, H):
     m.absorb(gd.q, gd.w_uk)
     torch.cuda.synchronize()
     hi = m.q_lat().float().cpu()
-    lo = m.q_lo().float().cpu()
+    lo = q_lo_values(m)
     ref = torch.einsum("bthk,hkl->bthl", inp.q[..., :128].double(), inp.w_uk.double())
     ref = ref.reshape(-1, 512)
     got = hi[:, :512].double() + lo.double()
-    assert ((got - ref).abs() <= ref.abs() * 2.0 ** -16 + 2e-6).all()
+    assert ((got - ref).abs() <= ref.abs() * 2.0 ** -13 + 2.0 ** -19 + 2e-6).all()
     assert torch.equal(hi[:, 512:], inp.q[..., 128:].reshape(-1, 64).float())
     assert (hi[:, :512].double() - ref).abs().max().item() <= ref.abs().max().item() * 2 ** -8
     out, lse, _ = run_gpu(inp)
