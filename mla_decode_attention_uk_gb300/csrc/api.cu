@@ -20,7 +20,8 @@ cudaError_t launch_plan(const int32_t* seq_lens, int B, int T, int max_pages, in
                         int32_t* seq_first, int32_t* seq_nsplit, int32_t* seq_slot,
                         int32_t* seq_len_eff, int32_t* prefix, cudaStream_t stream);
 int bmm_token_tile(int BT, bool absorb);
-cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q, int BT, int H,
+cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q,
+                          const CUtensorMap* tm_qlat, const CUtensorMap* tm_qlo, int BT, int H,
                           const __nv_bfloat16* q, __nv_bfloat16* qlat, uint8_t* qlo,
                           int32_t* status, cudaStream_t st, const uint8_t* wuk8,
                           const float* wuk_scale);
@@ -318,7 +319,17 @@ static int absorb_impl(const mla_decode_dims* d, const void* q, const void* w_uk
            : make_map(&tm_w, w_uk, static_cast<uint64_t>(H) * kNope, kLora, kLora, kBoxCols, 64,
                       false)))
     return MLA_DECODE_CUDA_ERROR;
-  return cuda_rc(launch_absorb(tm_w, tm_q, BT, H, static_cast<const __nv_bfloat16*>(q),
+  // More than 128 tokens with bf16 weights: the absorb kernel stores q_lat
+  // and q_lo by TMA, as 2-D views [tokens, heads x row] with 128-token boxes.
+  CUtensorMap tm_hi, tm_lo;
+  const bool rows = !w8 && bmm_token_tile(BT, true) == 128;
+  if (rows && !(make_map(&tm_hi, at<void>(ws, L.qlat), BT, static_cast<uint64_t>(H) * kDqk,
+                         static_cast<uint64_t>(H) * kDqk, kBoxCols, 128, false) &&
+                make_map(&tm_lo, at<void>(ws, L.qlo), BT, static_cast<uint64_t>(H) * kLora,
+                         static_cast<uint64_t>(H) * kLora, 128, 128, false, 1)))
+    return MLA_DECODE_CUDA_ERROR;
+  return cuda_rc(launch_absorb(tm_w, tm_q, rows ? &tm_hi : nullptr, rows ? &tm_lo : nullptr, BT,
+                               H, static_cast<const __nv_bfloat16*>(q),
                                at<__nv_bfloat16>(ws, L.qlat), at<uint8_t>(ws, L.qlo),
                                at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream), w8,
                                w8_scale));

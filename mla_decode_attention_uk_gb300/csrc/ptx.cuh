@@ -145,6 +145,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+// 2-D tiled store of one box from shared memory; completion is tracked by
+// bulk groups (commit, then wait until the copies have read shared memory).
+// Coordinates past the tensor's extent are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int32_t c0, int32_t c1,
+                                             uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+               ::"l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* m, int32_t c0,
                                                  int32_t c1, uint32_t bar, uint64_t policy) {
   asm volatile(
