@@ -24,7 +24,7 @@ cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q,
                           const CUtensorMap* tm_qlat, const CUtensorMap* tm_qlo, int BT, int H,
                           const __nv_bfloat16* q, __nv_bfloat16* qlat, uint8_t* qlo,
                           int32_t* status, cudaStream_t st, const uint8_t* wuk8,
-                          const float* wuk_scale);
+                          const float* wuk_scale, int sm_count);
 cudaError_t launch_up_project(const CUtensorMap& tm_wuv, const CUtensorMap& tm_olat, int BT,
                               int H, __nv_bfloat16* out, int32_t* status, cudaStream_t st,
                               const uint8_t* wuv8, const float* wuv_scale, bool one_wave);
@@ -328,11 +328,14 @@ static int absorb_impl(const mla_decode_dims* d, const void* q, const void* w_uk
                 make_map(&tm_lo, at<void>(ws, L.qlo), BT, static_cast<uint64_t>(H) * kLora,
                          static_cast<uint64_t>(H) * kLora, 128, 128, false, 1)))
     return MLA_DECODE_CUDA_ERROR;
+  int sms = 0;
+  rc = sm_count(&sms);
+  if (rc) return rc;
   return cuda_rc(launch_absorb(tm_w, tm_q, rows ? &tm_hi : nullptr, rows ? &tm_lo : nullptr, BT,
                                H, static_cast<const __nv_bfloat16*>(q),
                                at<__nv_bfloat16>(ws, L.qlat), at<uint8_t>(ws, L.qlo),
                                at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream), w8,
-                               w8_scale));
+                               w8_scale, sms));
 }
 
 static int up_project_impl(const mla_decode_dims* d, const void* w_uv, const uint8_t* w8,

@@ -393,34 +393,47 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
 }
 
 // Absorb step for more than 128 tokens (bf16 weights): the untransposed
-// product D[tok, n] = sum_k X[tok, h, k] W_UK[h][k][n] with M = 128 tokens,
-// N = kN latent columns and all of K = 128 staged at once.  A is the token
-// tile of q_nope (K-major: the same TMA box the transposed kernel uses as B),
-// B a kN-wide slice of W_UK[h] (MN-major: kN / 64 boxes of 64 columns).  An
-// M = 128 accumulator holds token row i in TMEM lane i, so each thread of the
-// epilogue owns one token: it writes its q_lat columns and E4M3 residuals with
-// 16-byte stores into 128B-swizzled tiles (the idle operand stages), and TMA
-// tensor stores move whole 128-token boxes to global memory.  (Storing the
-// rows from registers instead puts 32 rows in every warp store instruction
-// and measured 44 -> 63 us for 512 tokens x 128 heads.)
-template <int kN>
-struct RowsSmem {
-  static constexpr int kXBytes = 128 * 128;           // 128 tokens x 64 k (16 KB)
-  static constexpr int kWBytes = (kN / 64) * kBoxBytes;  // 64 k x kN n
-  static constexpr int kStage = kXBytes + kWBytes;
-  static constexpr int kTotal = 2 * kStage + 1024;    // two 64-deep K stages + alignment
-};
+// product D[tok, n] = sum_k X[tok, h, k] W_UK[h][k][n], one unit of work per
+// (128-token tile, 128 latent columns, head), M = 128 tokens, N = 128, K = 128
+// in two 64-deep stages.  A is the token tile of q_nope (K-major: the same TMA
+// box the transposed kernel uses as B), B a 128-column slice of W_UK[h]
+// (MN-major: two boxes of 64 columns).  An M = 128 accumulator holds token row
+// i in TMEM lane i, so each epilogue thread owns one token: it converts its
+// row (bf16 q_lat and the E4M3 residual) and writes it with 16-byte stores
+// into 128B-swizzled staging tiles, and TMA tensor stores move whole
+// 128-token boxes to global memory.  (Storing the rows from registers instead
+// puts 32 rows in every warp store instruction: 44 -> 63 us for 512 tokens x
+// 128 heads.)
+//
+// Persistent: one CTA per SM walks the units with a stride of the grid size,
+// through a ring of TMA stages, two TMEM accumulators and two staging
+// buffers, so the loads and MMAs of the next unit overlap the conversion and
+// stores of the current one (one unit per short-lived CTA left the SMs waiting
+// on memory: 16 % of warps active, DRAM at a third of its peak).  Its shared
+// memory (193 KB) leaves room for the planner, which runs at the same time.
+//   warp 0: TMA producer; warp 1: TMEM owner and MMA issuer; warps 2-9:
+//   epilogue (TMEM lane quarter = warp % 4, two warps per quarter splitting
+//   the columns, so each SM sub-partition has two to switch between), q_pe
+//   pass-through and the tensor stores.
+constexpr int kArThreads = 320;
+constexpr int kArEpiThreads = kArThreads - 64;
+constexpr int kArStages = 3;
+constexpr int kArXBytes = 128 * 128;                       // 128 tokens x 64 k
+constexpr int kArStageBytes = kArXBytes + 2 * kBoxBytes;   // + 64 k x 128 n: 32 KB
+constexpr int kArHiBytes = 2 * 128 * 128;                  // 128 tokens x 128 n, bf16
+constexpr int kArLoBytes = 128 * 128;                      // 128 tokens x 128 n, E4M3
+constexpr int kArOutBytes = kArHiBytes + kArLoBytes;
+constexpr int kArSmem = kArStages * kArStageBytes + 2 * kArOutBytes + 1024;
 
-template <int kN>
-__global__ void __launch_bounds__(kBmmThreads)
+__global__ void __launch_bounds__(kArThreads, 1)
 absorb_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                    const __grid_constant__ CUtensorMap tm_hi,
                    const __grid_constant__ CUtensorMap tm_lo, int BT, int H,
                    const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out_hi,
                    int32_t* __restrict__ status) {
-  using S = RowsSmem<kN>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[2], done_bar;
+  __shared__ __align__(8) uint64_t full_bar[kArStages], empty_bar[kArStages], acc_full[2],
+      acc_empty[2], drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -429,15 +442,27 @@ absorb_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
   // planner) comes just before exiting.
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tok0 = blockIdx.x * 128;
-  const int n0 = blockIdx.y * kN;
-  const int h = blockIdx.z;
+  const int ntt = (BT + 127) / 128;
+  const int units = ntt * (kLora / 128) * H;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sout = sbase + kArStages * kArStageBytes;
+  // Unit u: token tile u % ntt, latent block (u / ntt) % 4, head u / (4 ntt).
+  auto coords = [&](int u, int& tok0, int& n0, int& h) {
+    tok0 = (u % ntt) * 128;
+    n0 = ((u / ntt) % (kLora / 128)) * 128;
+    h = u / (ntt * (kLora / 128));
+  };
 
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&full_bar[0]), 1);
-    mbar_init(smem_u32(&full_bar[1]), 1);
-    mbar_init(smem_u32(&done_bar), 1);
+    for (int s = 0; s < kArStages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(smem_u32(&acc_full[j]), 1);
+      mbar_init(smem_u32(&acc_empty[j]), kArEpiThreads / 32);
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
     abort_sh = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_w);
@@ -445,8 +470,8 @@ absorb_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
     tma_prefetch_desc(&tm_hi);
     tma_prefetch_desc(&tm_lo);
   }
-  if (warp == 2) {
-    tmem_alloc(smem_u32(&tmem_base_sh), kN);
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 256);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -456,133 +481,173 @@ absorb_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
 
   if (warp == 0) {
     if (elect_one()) {
-      for (int kc = 0; kc < 2; ++kc) {
-        const uint32_t x = sbase + kc * S::kStage;
-        const uint32_t fb = smem_u32(&full_bar[kc]);
-        mbar_expect_tx(fb, S::kStage);
-        tma_load_2d(x, &tm_x, h * kDq + kc * 64, tok0, fb);
-#pragma unroll
-        for (int j = 0; j < kN / 64; ++j)
-          tma_load_2d(x + S::kXBytes + j * kBoxBytes, &tm_w, n0 + 64 * j, h * kNope + kc * 64, fb);
+      int g = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        int tok0, n0, h;
+        coords(u, tok0, n0, h);
+        for (int kc = 0; kc < 2; ++kc, ++g) {
+          const int s = g % kArStages;
+          if (g >= kArStages &&
+              !mbar_wait(smem_u32(&empty_bar[s]), ((g / kArStages) - 1) & 1, &abort_sh, status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t x = sbase + s * kArStageBytes;
+          const uint32_t fb = smem_u32(&full_bar[s]);
+          mbar_expect_tx(fb, kArStageBytes);
+          tma_load_2d(x, &tm_x, h * kDq + kc * 64, tok0, fb);
+          tma_load_2d(x + kArXBytes, &tm_w, n0, h * kNope + kc * 64, fb);
+          tma_load_2d(x + kArXBytes + kBoxBytes, &tm_w, n0 + 64, h * kNope + kc * 64, fb);
+        }
       }
+      // Copies still in flight (only after a timeout) land before the CTA
+      // exits: wait for the last load of each stage.
+      for (int j = g > kArStages ? g - kArStages : 0; j < g; ++j)
+        mbar_wait_drain(smem_u32(&full_bar[j % kArStages]), (j / kArStages) & 1, status);
     }
   } else if (warp == 1) {
     if (elect_one()) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, kN, /*a_mn=*/false, /*b_mn=*/true);
-      for (int kc = 0; kc < 2; ++kc) {
-        if (!mbar_wait(smem_u32(&full_bar[kc]), 0, &abort_sh, status)) break;
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128, /*a_mn=*/false, /*b_mn=*/true);
+      int g = 0, i = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
+        const int j = i & 1;
+        if (i >= 2 &&
+            !mbar_wait(smem_u32(&acc_empty[j]), ((i >> 1) - 1) & 1, &abort_sh, status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        const uint32_t x = sbase + kc * S::kStage;
+        for (int kc = 0; kc < 2; ++kc, ++g) {
+          const int s = g % kArStages;
+          if (!mbar_wait(smem_u32(&full_bar[s]), (g / kArStages) & 1, &abort_sh, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t x = sbase + s * kArStageBytes;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // 16 k per MMA: 32 bytes along a token row of A, 16 rows of B.
-          const uint64_t ad = sdesc_sw128(x + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(x + S::kXBytes + kk * 2048, kBoxBytes, 1024);
-          umma_bf16(tmem, ad, bd, idesc, (kc | kk) != 0);
+          for (int kk = 0; kk < 4; ++kk) {
+            // 16 k per MMA: 32 bytes along a token row of A, 16 rows of B.
+            const uint64_t ad = sdesc_sw128(x + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(x + kArXBytes + kk * 2048, kBoxBytes, 1024);
+            umma_bf16(tmem + 128 * j, ad, bd, idesc, (kc | kk) != 0);
+          }
+          umma_commit(smem_u32(&empty_bar[s]));
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&acc_full[j]));
+      }
+      // Drain this thread's MMAs before TMEM is released.
+      umma_commit(smem_u32(&drain_bar));
+      mbar_wait_drain(smem_u32(&drain_bar), 0, status);
+    }
+  } else {
+    // Epilogue: thread (quarter q4 = warp % 4, lane) owns token row
+    // r = 32 q4 + lane of each unit's tile (TMEM lane r); warps 2-5 take its
+    // columns 0-63, warps 6-9 columns 64-127.  Per 32 columns: one TMEM load,
+    // then 64 bytes of bf16 q_lat and 32 bytes of E4M3 residual
+    // (q_lat - bf16(q_lat)) * 2^10 into the unit's staging buffer, whose
+    // 128-byte rows hold 16-byte chunk c at c ^ (r & 7) (the 128B swizzle the
+    // tensor stores expect; a warp's stores then hit eight distinct chunk
+    // positions per eight rows).
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const int c0 = warp < 6 ? 0 : 2;      // first of this warp's two 32-column chunks
+    const int et = threadIdx.x - 64;      // 0 .. kArEpiThreads - 1
+    const uint32_t rsw = static_cast<uint32_t>(r & 7);
+    constexpr int kPeIters = 128 * 8 / kArEpiThreads;
+    int i = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
+      int tok0, n0, h;
+      coords(u, tok0, n0, h);
+      const int j = i & 1;
+      const uint32_t hi_t = sout + j * kArOutBytes, lo_t = hi_t + kArHiBytes;
+      // The first latent block's unit also passes q_pe through into columns
+      // 512..575 of q_lat: loads now, stores once the tile is out.
+      const bool pe = n0 == 0;
+      uint4 pv[kPeIters];
+      if (pe) {
+#pragma unroll
+        for (int it = 0; it < kPeIters; ++it) {
+          const int idx = et + it * kArEpiThreads, tl = idx >> 3, ch = idx & 7;
+          if (tok0 + tl < BT)
+            pv[it] = *reinterpret_cast<const uint4*>(
+                q + (static_cast<size_t>(tok0 + tl) * H + h) * kDq + kNope + ch * 8);
         }
       }
-      umma_commit(smem_u32(&done_bar));
-    }
-  } else if (blockIdx.y == 0) {
-    // Warps 2-3 of the first n block copy q_pe into columns 512..575 of q_lat
-    // while the MMAs run, all loads before the stores.
-    constexpr int kIters = 128 * 8 / 64;
-    const int nchunks = min(128, BT - tok0) * 8;
-    const int t0 = threadIdx.x - 64;
-    uint4 v[kIters];
+      const bool ok = mbar_wait(smem_u32(&acc_full[j]), (i >> 1) & 1, &abort_sh, status);
+      // Staging buffer j was last read by the tensor stores of unit i - 2;
+      // only those of unit i - 1 may still be reading.
+      if (et == 0) tma_store_wait_read_all_but_last();
+      if (!named_bar_and(1, kArEpiThreads, ok)) break;
+      tc_fence_after();
 #pragma unroll
-    for (int it = 0; it < kIters; ++it) {
-      const int i = t0 + it * 64;
-      if (i < nchunks) {
-        const size_t row = static_cast<size_t>(tok0 + (i >> 3)) * H + h;
-        v[it] = *reinterpret_cast<const uint4*>(q + row * kDq + kNope + (i & 7) * 8);
+      for (int c = c0; c < c0 + 2; ++c) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem + 128 * j + (static_cast<uint32_t>(q4 * 32) << 16) + c * 32, v);
+        tmem_wait_ld();
+        uint32_t hw[16], lw[8];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float v0 = __uint_as_float(v[2 * e]), v1 = __uint_as_float(v[2 * e + 1]);
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(v0, v1);
+          hw[e] = *reinterpret_cast<const uint32_t*>(&hv);
+          const float2 hf = __bfloat1622float2(hv);
+          // Two residuals per conversion, the first in the low byte.
+          const uint32_t pair = __nv_cvt_float2_to_fp8x2(
+              make_float2((v0 - hf.x) * kQloScale, (v1 - hf.y) * kQloScale), __NV_SATFINITE,
+              __NV_E4M3);
+          if (e & 1)
+            lw[e >> 1] |= pair << 16;
+          else
+            lw[e >> 1] = pair;
+        }
+        // hi: box c / 2, chunks 4 (c % 2) .. + 3;  lo: chunks 2 c, 2 c + 1.
+        const uint32_t hrow = hi_t + (c >> 1) * (128 * 128) + r * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          st_shared_v4(hrow + (((4 * (c & 1) + k) ^ rsw) << 4), hw[4 * k], hw[4 * k + 1],
+                       hw[4 * k + 2], hw[4 * k + 3]);
+        const uint32_t lrow = lo_t + r * 128;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          st_shared_v4(lrow + (((2 * c + k) ^ rsw) << 4), lw[4 * k], lw[4 * k + 1],
+                       lw[4 * k + 2], lw[4 * k + 3]);
+      }
+      // The accumulator goes back to the MMA issuer, the staging tiles to the
+      // tensor stores (rows past the last token are clipped by the maps).
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[j]));
+      fence_proxy_async_smem();
+      named_bar_sync(1, kArEpiThreads);
+      if (et == 0) {
+        tma_store_2d(&tm_hi, h * kDqk + n0, tok0, hi_t);
+        tma_store_2d(&tm_hi, h * kDqk + n0 + 64, tok0, hi_t + 128 * 128);
+        tma_store_2d(&tm_lo, h * kLora + n0, tok0, lo_t);
+        tma_store_commit();
+      }
+      if (pe) {
+#pragma unroll
+        for (int it = 0; it < kPeIters; ++it) {
+          const int idx = et + it * kArEpiThreads, tl = idx >> 3, ch = idx & 7;
+          if (tok0 + tl < BT)
+            *reinterpret_cast<uint4*>(out_hi + (static_cast<size_t>(tok0 + tl) * H + h) * kDqk +
+                                      kLora + ch * 8) = pv[it];
+        }
       }
     }
-#pragma unroll
-    for (int it = 0; it < kIters; ++it) {
-      const int i = t0 + it * 64;
-      if (i < nchunks) {
-        const size_t row = static_cast<size_t>(tok0 + (i >> 3)) * H + h;
-        *reinterpret_cast<uint4*>(out_hi + row * kDqk + kLora + (i & 7) * 8) = v[it];
-      }
-    }
+    // Shared memory must outlive the tensor stores' reads.
+    if (et == 0) tma_store_wait_read();
   }
   __syncwarp();
-
-  // Epilogue: thread (warp w, lane i) owns token row r = 32 w + i of the tile
-  // (TMEM lane r).  Per 32 columns: one TMEM load, then 64 bytes of bf16 q_lat
-  // and 32 bytes of E4M3 residual (q_lat - bf16(q_lat)) * 2^10 into the
-  // staging tiles, whose 128-byte rows hold 16-byte chunk c at c ^ (r & 7)
-  // (the 128B swizzle the tensor stores expect; a warp's stores then hit
-  // eight distinct chunk positions per eight rows).  The operand stages are
-  // free once the MMAs are done: hi tiles (kN / 64 boxes of 64 columns) first,
-  // then lo tiles (kN / 128 boxes of 128 bytes).
-  const bool have = mbar_wait(smem_u32(&done_bar), 0, &abort_sh, status);
-  tc_fence_after();
-  const int r = warp * 32 + lane;
-  const uint32_t hi_tile = sbase, lo_tile = sbase + (kN / 64) * 128 * 128;
-  // The TMEM loads below are warp-collective: the warp goes on only together.
-  const bool go = __all_sync(0xffffffffu, have && !abort_sh);
-  if (go) {
-    const uint32_t rsw = static_cast<uint32_t>(r & 7);
-#pragma unroll 1
-    for (int c = 0; c < kN / 32; ++c) {
-      uint32_t v[32];
-      tmem_ld_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c * 32, v);
-      tmem_wait_ld();
-      uint32_t hw[16], lw[8];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float v0 = __uint_as_float(v[2 * j]), v1 = __uint_as_float(v[2 * j + 1]);
-        const __nv_bfloat162 hv = __floats2bfloat162_rn(v0, v1);
-        hw[j] = *reinterpret_cast<const uint32_t*>(&hv);
-        const uint32_t l0 = __nv_cvt_float_to_fp8((v0 - __low2float(hv)) * kQloScale,
-                                                  __NV_SATFINITE, __NV_E4M3);
-        const uint32_t l1 = __nv_cvt_float_to_fp8((v1 - __high2float(hv)) * kQloScale,
-                                                  __NV_SATFINITE, __NV_E4M3);
-        const uint32_t pair = l0 | (l1 << 8);
-        if (j & 1)
-          lw[j >> 1] |= pair << 16;
-        else
-          lw[j >> 1] = pair;
-      }
-      // hi: box c / 2, chunks 4 (c % 2) .. + 3;  lo: box c / 4, chunks 2 (c % 4) .. + 1.
-      const uint32_t hrow = hi_tile + (c >> 1) * (128 * 128) + r * 128;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        st_shared_v4(hrow + (((4 * (c & 1) + i) ^ rsw) << 4), hw[4 * i], hw[4 * i + 1],
-                     hw[4 * i + 2], hw[4 * i + 3]);
-      const uint32_t lrow = lo_tile + (c >> 2) * (128 * 128) + r * 128;
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-        st_shared_v4(lrow + (((2 * (c & 3) + i) ^ rsw) << 4), lw[4 * i], lw[4 * i + 1],
-                     lw[4 * i + 2], lw[4 * i + 3]);
-    }
-    fence_proxy_async_smem();  // the tensor stores read what these threads wrote
-  }
-  __syncthreads();
-  if (go && threadIdx.x == 0) {
-    // Rows past the last token are clipped by the tensor maps.
-#pragma unroll
-    for (int j = 0; j < kN / 64; ++j)
-      tma_store_2d(&tm_hi, h * kDqk + n0 + 64 * j, tok0, hi_tile + j * (128 * 128));
-#pragma unroll
-    for (int j = 0; j < kN / 128; ++j)
-      tma_store_2d(&tm_lo, h * kLora + n0 + 128 * j, tok0, lo_tile + j * (128 * 128));
-    tma_store_commit();
-    tma_store_wait_read();  // shared memory must outlive the copies' reads
-  }
-  // After a timeout the copies may not all have been waited for: let both
-  // stages land before the CTA exits (at once otherwise).
-  if (threadIdx.x == 0) {
-    mbar_wait_drain(smem_u32(&full_bar[0]), 0, status);
-    mbar_wait_drain(smem_u32(&full_bar[1]), 0, status);
-  }
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kN);
+    tmem_dealloc(tmem, 256);
   }
   griddep_wait();
 }
@@ -609,18 +674,16 @@ cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, 
   return cudaGetLastError();
 }
 
-template <int kN>
 cudaError_t launch_absorb_rows(const CUtensorMap& tw, const CUtensorMap& tx,
                                const CUtensorMap& thi, const CUtensorMap& tlo, int BT, int H,
                                const __nv_bfloat16* q, __nv_bfloat16* hi, int32_t* status,
-                               cudaStream_t st) {
-  constexpr int smem = RowsSmem<kN>::kTotal;
-  cudaError_t e = cudaFuncSetAttribute(absorb_rows_kernel<kN>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                               int sm_count, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(absorb_rows_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kArSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid((BT + 127) / 128, kLora / kN, H);
-  e = launch_pdl(absorb_rows_kernel<kN>, grid, dim3(kBmmThreads), smem, st, tw, tx, thi, tlo, BT,
-                 H, q, hi, status);
+  const int units = (BT + 127) / 128 * (kLora / 128) * H;
+  e = launch_pdl(absorb_rows_kernel, dim3(units < sm_count ? units : sm_count), dim3(kArThreads),
+                 kArSmem, st, tw, tx, thi, tlo, BT, H, q, hi, status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -644,14 +707,13 @@ cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q,
                           const CUtensorMap* tm_qlat, const CUtensorMap* tm_qlo, int BT, int H,
                           const __nv_bfloat16* q, __nv_bfloat16* qlat, uint8_t* qlo,
                           int32_t* status, cudaStream_t st, const uint8_t* wuk8,
-                          const float* wuk_scale) {
+                          const float* wuk_scale, int sm_count) {
   const Fp8Weights w8{wuk8, wuk_scale, kLora};
   // More than 128 tokens (128-token boxes) with bf16 weights: the
   // untransposed kernel, given output tensor maps for q_lat and q_lo.
-  // 128 latent columns per CTA (three CTAs per SM) measured faster than 256
-  // (two per SM): 512 tokens x 128 heads, step 331.1 -> 327.4 us.
   if (tm_qlat && tm_qlo)
-    return launch_absorb_rows<128>(tm_wuk, tm_q, *tm_qlat, *tm_qlo, BT, H, q, qlat, status, st);
+    return launch_absorb_rows(tm_wuk, tm_q, *tm_qlat, *tm_qlo, BT, H, q, qlat, status, sm_count,
+                              st);
   switch (bmm_token_tile(BT, true)) {
     case 16: return launch_bmm_nt<BmmMode::kAbsorb, 16>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st, w8);
     case 32: return launch_bmm_nt<BmmMode::kAbsorb, 32>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st, w8);
