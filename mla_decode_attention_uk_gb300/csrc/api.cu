@@ -311,18 +311,19 @@ static int absorb_impl(const mla_decode_dims* d, const void* q, const void* w_uk
   if (rc) return rc;
   const int BT = d->batch * d->q_len, H = d->num_heads;
   CUtensorMap tm_q, tm_w;
+  // 128 tokens or more with bf16 weights: the untransposed absorb kernel,
+  // which stores q_lat and q_lo by TMA as 2-D views [tokens, heads x row]
+  // and reads 128-token boxes of q.
+  const bool rows = !w8 && BT >= 128;
   if (!make_map(&tm_q, q, BT, static_cast<uint64_t>(H) * kDq, static_cast<uint64_t>(H) * kDq,
-                kBoxCols, bmm_token_tile(BT, true), false))
+                kBoxCols, rows ? 128 : bmm_token_tile(BT, true), false))
     return MLA_DECODE_CUDA_ERROR;
   // FP8 weights: 128-byte boxes of 128 m values x 64 k rows.
   if (!(w8 ? make_map(&tm_w, w8, static_cast<uint64_t>(H) * kNope, kLora, kLora, 128, 64, false, 1)
            : make_map(&tm_w, w_uk, static_cast<uint64_t>(H) * kNope, kLora, kLora, kBoxCols, 64,
                       false)))
     return MLA_DECODE_CUDA_ERROR;
-  // More than 128 tokens with bf16 weights: the absorb kernel stores q_lat
-  // and q_lo by TMA, as 2-D views [tokens, heads x row] with 128-token boxes.
   CUtensorMap tm_hi, tm_lo;
-  const bool rows = !w8 && bmm_token_tile(BT, true) == 128;
   if (rows && !(make_map(&tm_hi, at<void>(ws, L.qlat), BT, static_cast<uint64_t>(H) * kDqk,
                          static_cast<uint64_t>(H) * kDqk, kBoxCols, 128, false) &&
                 make_map(&tm_lo, at<void>(ws, L.qlo), BT, static_cast<uint64_t>(H) * kLora,
