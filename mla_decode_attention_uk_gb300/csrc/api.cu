@@ -311,10 +311,10 @@ static int absorb_impl(const mla_decode_dims* d, const void* q, const void* w_uk
   if (rc) return rc;
   const int BT = d->batch * d->q_len, H = d->num_heads;
   CUtensorMap tm_q, tm_w;
-  // 128 tokens or more with bf16 weights: the untransposed absorb kernel,
+  // 128 tokens or more: the untransposed absorb kernel,
   // which stores q_lat and q_lo by TMA as 2-D views [tokens, heads x row]
   // and reads 128-token boxes of q.
-  const bool rows = !w8 && BT >= 128;
+  const bool rows = BT >= 128;
   if (!make_map(&tm_q, q, BT, static_cast<uint64_t>(H) * kDq, static_cast<uint64_t>(H) * kDq,
                 kBoxCols, rows ? 128 : bmm_token_tile(BT, true), false))
     return MLA_DECODE_CUDA_ERROR;

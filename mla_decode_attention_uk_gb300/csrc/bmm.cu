@@ -9,7 +9,7 @@
 //
 // Both run transposed on the tensor cores so the weight dimension fills the
 // 128-row MMA and the (often small) token count is the N dimension (the
-// absorb step with bf16 weights and 128 tokens or more runs untransposed
+// absorb step with 128 tokens or more runs untransposed
 // instead; see absorb_rows_kernel):
 //   D[m, tok] = sum_k W[h][k][m] * X[tok, h, k]
 // A = a 128-wide slice of W[h] (MN-major, staged by TMA with 128B swizzle),
@@ -98,6 +98,39 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return v;
+}
+
+// One converter thread's share of a raw FP8 weight tile: k row kr, m (or n)
+// columns 64 half .. 64 half + 63.  The raw tile arrives by TMA with 128B
+// swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)); the bf16 tile is
+// written in the layout TMA gives a bf16 weight tile: two 64-column boxes
+// (one per half), 128-byte rows, same swizzle.  The two halves of a row visit
+// their chunks in opposite order (jj = j ^ 2 half), so a quarter-warp's
+// 16-byte reads and writes fall on eight distinct chunk positions: no bank
+// conflicts.
+__device__ __forceinline__ void convert_fp8_row(uint32_t raw_tile, uint32_t bf16_tile, int kr,
+                                                int half, float sc) {
+  const uint32_t rrow = raw_tile + kr * 128;
+  const uint32_t arow = bf16_tile + half * kBoxBytes + kr * 128;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {  // 16 weights per 16-byte chunk
+    const int jj = j ^ (half << 1);
+    const int qd = half * 4 + jj;
+    const uint4 raw = ld_shared_v4(rrow + ((qd ^ (kr & 7)) << 4));
+    const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t ow[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {  // two E4M3 values -> one bf16 pair
+      const __nv_fp8x2_storage_t pr =
+          static_cast<__nv_fp8x2_storage_t>((rw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+      const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
+      const __nv_bfloat162 bv = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+      ow[e] = *reinterpret_cast<const uint32_t*>(&bv);
+    }
+    const int c0 = 2 * jj;
+    st_shared_v4(arow + ((c0 ^ (kr & 7)) << 4), ow[0], ow[1], ow[2], ow[3]);
+    st_shared_v4(arow + (((c0 + 1) ^ (kr & 7)) << 4), ow[4], ow[5], ow[6], ow[7]);
+  }
 }
 
 template <BmmMode MODE, int NT, int STAGES, bool W8>
@@ -200,13 +233,8 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
     }
   } else if (W8 && warp >= 2 && warp < 6) {
     // FP8 weight converters: thread ct (0..127) owns m columns 64 half ..
-    // 64 half + 63 of k row kr of each stage's 64 x 128 weight tile.  Raw
-    // tiles arrive by TMA with 128B swizzle (16-byte chunk c of row r at chunk
-    // c ^ (r & 7)).  The bf16 tile is written in the layout TMA gives a bf16
-    // W: two 64-column m boxes (one per half), 128-byte rows, same swizzle.
-    // The two halves of a row visit their chunks in opposite order (jj =
-    // j ^ 2 half), so a quarter-warp's 16-byte reads and writes fall on eight
-    // distinct chunk positions: no bank conflicts.
+    // 64 half + 63 of k row kr of each stage's 64 x 128 weight tile
+    // (convert_fp8_row).
     const int ct = threadIdx.x - 64;
     const int kr = ct >> 1, half = ct & 1;
     const uint32_t raw0 = sbase + S::kPipe;
@@ -231,29 +259,9 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
         ok = mbar_wait(smem_u32(&empty_bar[s]), ((kc / STAGES) - 1) & 1, &abort_sh, status);
       if (ok) ok = mbar_wait(smem_u32(&raw_bar[r]), (kc / kRing) & 1, &abort_sh, status);
       if (!named_bar_and(1, 128, ok)) break;
-      const uint32_t rrow = raw0 + r * kRawBytes + kr * 128;
-      const uint32_t arow = sbase + s * S::kStageBytes + half * kBoxBytes + kr * 128;
       const int kb = kc >> 1;  // 128-row scale block of this 64-row tile
       const float sc = kb == 0 ? scl[0] : kb == 1 ? scl[1] : kb == 2 ? scl[2] : scl[3];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {  // 16 weights (m) per 16-byte chunk
-        const int jj = j ^ (half << 1);
-        const int qd = half * 4 + jj;
-        const uint4 raw = ld_shared_v4(rrow + ((qd ^ (kr & 7)) << 4));
-        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t ow[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {  // two E4M3 values -> one bf16 pair
-          const __nv_fp8x2_storage_t pr =
-              static_cast<__nv_fp8x2_storage_t>((rw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
-          const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
-          const __nv_bfloat162 bv = __floats2bfloat162_rn(f.x * sc, f.y * sc);
-          ow[e] = *reinterpret_cast<const uint32_t*>(&bv);
-        }
-        const int c0 = 2 * jj;
-        st_shared_v4(arow + ((c0 ^ (kr & 7)) << 4), ow[0], ow[1], ow[2], ow[3]);
-        st_shared_v4(arow + (((c0 + 1) ^ (kr & 7)) << 4), ow[4], ow[5], ow[6], ow[7]);
-      }
+      convert_fp8_row(raw0 + r * kRawBytes, sbase + s * S::kStageBytes, kr, half, sc);
       // The bf16 tile goes to the tensor core and raw tile r back to TMA:
       // order these threads' shared-memory accesses before both.
       fence_proxy_async_smem();
@@ -392,7 +400,7 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
   if constexpr (MODE == BmmMode::kAbsorb) griddep_wait();
 }
 
-// Absorb step for 128 tokens or more (bf16 weights): the untransposed
+// Absorb step for 128 tokens or more: the untransposed
 // product D[tok, n] = sum_k X[tok, h, k] W_UK[h][k][n], one unit of work per
 // (128-token tile, 128 latent columns, head), M = 128 tokens, N = 128, K = 128
 // in two 64-deep stages.  A is the token tile of q_nope (K-major: the same TMA
@@ -415,25 +423,40 @@ bmm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUt
 //   epilogue (TMEM lane quarter = warp % 4, two warps per quarter splitting
 //   the columns, so each SM sub-partition has two to switch between), q_pe
 //   pass-through and the tensor stores.
-constexpr int kArThreads = 320;
-constexpr int kArEpiThreads = kArThreads - 64;
+//
+// FP8 weights (W8): each stage also holds the raw 64 k x 128 n FP8 tile,
+// and warps 10-13 decompress it, W = bf16(fp32(w8) * scale), into the
+// stage's B operand, which has exactly the layout of the transposed kernel's
+// bf16 weight tile (two 64-column boxes of 64 k rows, 128B swizzle), so the
+// same conversion applies.  One staging buffer keeps the shared memory
+// (169 KB) clear of the planner's.
+constexpr int kArEpiThreads = 256;                         // warps 2-9
 constexpr int kArStages = 3;
 constexpr int kArXBytes = 128 * 128;                       // 128 tokens x 64 k
 constexpr int kArStageBytes = kArXBytes + 2 * kBoxBytes;   // + 64 k x 128 n: 32 KB
 constexpr int kArHiBytes = 2 * 128 * 128;                  // 128 tokens x 128 n, bf16
 constexpr int kArLoBytes = 128 * 128;                      // 128 tokens x 128 n, E4M3
 constexpr int kArOutBytes = kArHiBytes + kArLoBytes;
-constexpr int kArSmem = kArStages * kArStageBytes + 2 * kArOutBytes + 1024;
+template <bool W8>
+struct RowsCfg {
+  static constexpr int kThreads = 64 + kArEpiThreads + (W8 ? 128 : 0);
+  static constexpr int kRawStage = W8 ? kRawBytes : 0;  // raw FP8 tile per stage
+  static constexpr int kOutBufs = W8 ? 1 : 2;
+  static constexpr int kSmem =
+      kArStages * (kArStageBytes + kRawStage) + kOutBufs * kArOutBytes + 1024;
+};
 
-__global__ void __launch_bounds__(kArThreads, 1)
+template <bool W8>
+__global__ void __launch_bounds__(RowsCfg<W8>::kThreads, 1)
 absorb_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                    const __grid_constant__ CUtensorMap tm_hi,
                    const __grid_constant__ CUtensorMap tm_lo, int BT, int H,
                    const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out_hi,
-                   int32_t* __restrict__ status) {
+                   int32_t* __restrict__ status, const float* __restrict__ w8_scale) {
+  using C = RowsCfg<W8>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kArStages], empty_bar[kArStages], acc_full[2],
-      acc_empty[2], drain_bar;
+  __shared__ __align__(8) uint64_t full_bar[kArStages], empty_bar[kArStages],
+      conv_bar[W8 ? kArStages : 1], acc_full[2], acc_empty[2], drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -445,7 +468,8 @@ absorb_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
   const int ntt = (BT + 127) / 128;
   const int units = ntt * (kLora / 128) * H;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t sout = sbase + kArStages * kArStageBytes;
+  const uint32_t raw0 = sbase + kArStages * kArStageBytes;  // raw FP8 tiles (W8)
+  const uint32_t sout = raw0 + kArStages * C::kRawStage;
   // Unit u: token tile u % ntt, latent block (u / ntt) % 4, head u / (4 ntt).
   auto coords = [&](int u, int& tok0, int& n0, int& h) {
     tok0 = (u % ntt) * 128;
@@ -457,6 +481,7 @@ absorb_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
     for (int s = 0; s < kArStages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
+      if constexpr (W8) mbar_init(smem_u32(&conv_bar[s]), 1);
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(smem_u32(&acc_full[j]), 1);
@@ -495,10 +520,14 @@ absorb_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
           }
           const uint32_t x = sbase + s * kArStageBytes;
           const uint32_t fb = smem_u32(&full_bar[s]);
-          mbar_expect_tx(fb, kArStageBytes);
+          mbar_expect_tx(fb, W8 ? kArXBytes + C::kRawStage : kArStageBytes);
           tma_load_2d(x, &tm_x, h * kDq + kc * 64, tok0, fb);
-          tma_load_2d(x + kArXBytes, &tm_w, n0, h * kNope + kc * 64, fb);
-          tma_load_2d(x + kArXBytes + kBoxBytes, &tm_w, n0 + 64, h * kNope + kc * 64, fb);
+          if constexpr (W8) {
+            tma_load_2d(raw0 + s * C::kRawStage, &tm_w, n0, h * kNope + kc * 64, fb);
+          } else {
+            tma_load_2d(x + kArXBytes, &tm_w, n0, h * kNope + kc * 64, fb);
+            tma_load_2d(x + kArXBytes + kBoxBytes, &tm_w, n0 + 64, h * kNope + kc * 64, fb);
+          }
         }
       }
       // Copies still in flight (only after a timeout) land before the CTA
@@ -521,7 +550,8 @@ absorb_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         tc_fence_after();
         for (int kc = 0; kc < 2; ++kc, ++g) {
           const int s = g % kArStages;
-          if (!mbar_wait(smem_u32(&full_bar[s]), (g / kArStages) & 1, &abort_sh, status)) {
+          if (!mbar_wait(smem_u32(&full_bar[s]), (g / kArStages) & 1, &abort_sh, status) ||
+              (W8 && !mbar_wait(smem_u32(&conv_bar[s]), (g / kArStages) & 1, &abort_sh, status))) {
             ok = false;
             break;
           }
@@ -543,6 +573,33 @@ absorb_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
       umma_commit(smem_u32(&drain_bar));
       mbar_wait_drain(smem_u32(&drain_bar), 0, status);
     }
+  } else if (W8 && warp >= 2 + kArEpiThreads / 32) {
+    // FP8 converters (warps 10-13): thread ct owns k row ct / 2, columns
+    // 64 (ct % 2) .. + 63 of each stage's weight tile.
+    const int ct = threadIdx.x - 64 - kArEpiThreads;
+    int g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      int tok0, n0, h;
+      coords(u, tok0, n0, h);
+      // W_UK scales [H, 1, 4]: one per 128 x 128 block.
+      const float sc = __ldg(w8_scale + h * (kLora / 128) + n0 / 128);
+      for (int kc = 0; kc < 2; ++kc, ++g) {
+        const int s = g % kArStages;
+        ok = mbar_wait(smem_u32(&full_bar[s]), (g / kArStages) & 1, &abort_sh, status);
+        if (!named_bar_and(2, 128, ok)) {
+          ok = false;
+          break;
+        }
+        convert_fp8_row(raw0 + s * C::kRawStage, sbase + s * kArStageBytes + kArXBytes, ct >> 1,
+                        ct & 1, sc);
+        // The bf16 tile goes to the tensor core: order these threads' shared
+        // memory writes before it.
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (ct == 0) mbar_arrive(smem_u32(&conv_bar[s]));
+      }
+    }
   } else {
     // Epilogue: thread (quarter q4 = warp % 4, lane) owns token row
     // r = 32 q4 + lane of each unit's tile (TMEM lane r); warps 2-5 take its
@@ -563,7 +620,7 @@ absorb_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
       int tok0, n0, h;
       coords(u, tok0, n0, h);
       const int j = i & 1;
-      const uint32_t hi_t = sout + j * kArOutBytes, lo_t = hi_t + kArHiBytes;
+      const uint32_t hi_t = sout + (i % C::kOutBufs) * kArOutBytes, lo_t = hi_t + kArHiBytes;
       // The first latent block's unit also passes q_pe through into columns
       // 512..575 of q_lat: loads now, stores once the tile is out.
       const bool pe = n0 == 0;
@@ -578,9 +635,15 @@ absorb_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
         }
       }
       const bool ok = mbar_wait(smem_u32(&acc_full[j]), (i >> 1) & 1, &abort_sh, status);
-      // Staging buffer j was last read by the tensor stores of unit i - 2;
-      // only those of unit i - 1 may still be reading.
-      if (et == 0) tma_store_wait_read_all_but_last();
+      // With two staging buffers, buffer j was last read by the tensor stores
+      // of unit i - 2, and only those of unit i - 1 may still be reading;
+      // with one, unit i - 1's must be done.
+      if (et == 0) {
+        if constexpr (C::kOutBufs == 2)
+          tma_store_wait_read_all_but_last();
+        else
+          tma_store_wait_read();
+      }
       if (!named_bar_and(1, kArEpiThreads, ok)) break;
       tc_fence_after();
 #pragma unroll
@@ -674,16 +737,19 @@ cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, 
   return cudaGetLastError();
 }
 
+template <bool W8>
 cudaError_t launch_absorb_rows(const CUtensorMap& tw, const CUtensorMap& tx,
                                const CUtensorMap& thi, const CUtensorMap& tlo, int BT, int H,
                                const __nv_bfloat16* q, __nv_bfloat16* hi, int32_t* status,
-                               int sm_count, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(absorb_rows_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kArSmem);
+                               const float* w8_scale, int sm_count, cudaStream_t st) {
+  using C = RowsCfg<W8>;
+  cudaError_t e = cudaFuncSetAttribute(absorb_rows_kernel<W8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   const int units = (BT + 127) / 128 * (kLora / 128) * H;
-  e = launch_pdl(absorb_rows_kernel, dim3(units < sm_count ? units : sm_count), dim3(kArThreads),
-                 kArSmem, st, tw, tx, thi, tlo, BT, H, q, hi, status);
+  e = launch_pdl(absorb_rows_kernel<W8>, dim3(units < sm_count ? units : sm_count),
+                 dim3(C::kThreads), C::kSmem, st, tw, tx, thi, tlo, BT, H, q, hi, status,
+                 w8_scale);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -709,12 +775,14 @@ cudaError_t launch_absorb(const CUtensorMap& tm_wuk, const CUtensorMap& tm_q,
                           int32_t* status, cudaStream_t st, const uint8_t* wuk8,
                           const float* wuk_scale, int sm_count) {
   const Fp8Weights w8{wuk8, wuk_scale, kLora};
-  // 128 tokens or more with bf16 weights (measured: 128 tokens x 128 heads,
+  // 128 tokens or more (measured with bf16 weights, 128 tokens x 128 heads:
   // step 240.8 -> 238.5 us): the untransposed kernel, given output tensor
   // maps for q_lat and q_lo and 128-token boxes of q.
   if (tm_qlat && tm_qlo)
-    return launch_absorb_rows(tm_wuk, tm_q, *tm_qlat, *tm_qlo, BT, H, q, qlat, status, sm_count,
-                              st);
+    return wuk8 ? launch_absorb_rows<true>(tm_wuk, tm_q, *tm_qlat, *tm_qlo, BT, H, q, qlat,
+                                           status, wuk_scale, sm_count, st)
+                : launch_absorb_rows<false>(tm_wuk, tm_q, *tm_qlat, *tm_qlo, BT, H, q, qlat,
+                                            status, nullptr, sm_count, st);
   switch (bmm_token_tile(BT, true)) {
     case 16: return launch_bmm_nt<BmmMode::kAbsorb, 16>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st, w8);
     case 32: return launch_bmm_nt<BmmMode::kAbsorb, 32>(tm_wuk, tm_q, BT, H, kNope, kDq, kLora, q, qlat, qlo, status, st, w8);

@@ -49,10 +49,15 @@ def test_absorb_bmm_matches_fp32_matmul():
     assert (hi[:, :512].double() - ref).abs().max().item() <= ref.abs().max().item() * 2 ** -8
 
 
-@pytest.mark.parametrize("B,T,H", [(200, 2, 16), (130, 2, 128), (256, 1, 32)])
+@pytest.mark.parametrize("B,T,H", [(200, 2, 16), (130, 2, 128), (256, 1, 32), (64, 2, 16),
+                                   (129, 1, 48)])
 def test_absorb_bmm_large_token_counts_matches_fp64(B, T, H):
-    # 128-token tiles: 400 and 260 tokens leave a ragged last tile, 256 is two
-    # full ones; 16, 32 and 128 heads.  Same bound as the small case above.
+    # 128-token tiles of the untransposed absorb kernel: 400 and 260 tokens
+    # leave a ragged last tile, 256 is two full ones, 128 exactly one, and 129
+    # a last tile of one token (the tensor stores clip the other 127 rows);
+    # 16 to 128 heads, so the persistent grid has fewer units than SMs
+    # (128 tokens x 16 heads: 64 units) or several per SM (129 x 48: 384).
+    # Same bound as the small case above.
     g = torch.Generator().manual_seed(40 + B + H)
     lens = torch.randint(T, 200, (B,), generator=g).tolist()
     inp = make_inputs(B, lens, T, H, seed=42 + H)
