@@ -364,11 +364,11 @@ class WorkloadRunner:
         self.m.plan(self.g.seq_lens)
 
     def step(self):
+        # One decode step as a caller makes it: the plan, then the whole run
+        # (absorb, attend, combine, up-project) in one call.  The per-step
+        # calls above serve the --breakdown timings.
         self.plan()
-        self.absorb()
-        self.attend()
-        self.combine()
-        self.up_project()
+        self.run_all()
 
     def run_all(self):
         g, W = self.g, self.W

@@ -137,14 +137,22 @@ int mla_decode_plan_ex(const mla_decode_dims* dims, const int32_t* seq_lens,
  *   out         bf16 [B, T, H, 128] (written)
  *   lse         fp32 [B, T, H] (written): natural-log log-sum-exp of the
  *               scaled scores of each query row
- * Enqueues four kernels: absorb, attend, combine, up-project. */
+ * Enqueues four kernels: absorb, attend, combine, up-project.  For 128 tokens
+ * (B*T) or more in more (128-token, head) tiles than the GPU has SMs, the
+ * combine kernel merges split sequences only and the up-projection applies
+ * the first-order LSE correction of the other rows (it stages their o_lat
+ * and q_lo anyway); the result equals that of the four step calls below up
+ * to the summation order of that correction (lse within a few ulp; out
+ * bitwise). */
 int mla_decode_run(const mla_decode_dims* dims, const void* q, const void* kv_cache,
                    const int32_t* block_table, const int32_t* seq_lens, const void* w_uk,
                    const void* w_uv, float softmax_scale, void* out, float* lse,
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* The four steps of mla_decode_run as separate calls, in this order, on one
- * workspace after mla_decode_plan (for profiling one step at a time).
+ * workspace after mla_decode_plan (for profiling one step at a time; for
+ * large batches mla_decode_run moves part of the combine into its
+ * up-projection, see above).
  *   absorb:     q, w_uk            -> q_lat (bf16 part, and the residual q_lo
  *                                     as E4M3 of q_lo * 2^10, workspace)
  *   attend:     q_lat, cache, ...  -> o_lat + lse (from the bf16 part of q_lat)

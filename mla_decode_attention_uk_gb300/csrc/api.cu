@@ -38,10 +38,15 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
                           __nv_bfloat16* olat, float* lse,
                           int32_t* status, int B, int T, int H, int max_pages,
                           int num_pages, float scale, cudaStream_t st);
+cudaError_t launch_up_project_rows(const CUtensorMap& tm_wuv, const CUtensorMap& tm_olat,
+                                   const CUtensorMap& tm_qlo, const CUtensorMap& tm_out, int BT,
+                                   int T, int H, const int32_t* seq_nsplit, float* lse,
+                                   float scale, int32_t* status, const float* wuv_scale,
+                                   int sm_count, cudaStream_t st);
 cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, const void* ws,
                            const PlanHeader* header, const uint8_t* qlo,
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
-                           int splits_per_seq, cudaStream_t st);
+                           int splits_per_seq, int split_ranges, cudaStream_t st);
 }  // namespace mla
 
 namespace {
@@ -115,7 +120,8 @@ EncodeTiledFn encoder() {
 // `cols` (row stride `row_stride` elements), box = box_cols x box_rows,
 // 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t row_stride,
-              uint32_t box_cols, uint32_t box_rows, bool stream_hint, int elem_bytes = 2) {
+              uint32_t box_cols, uint32_t box_rows, bool stream_hint, int elem_bytes = 2,
+              bool swizzle = true) {
   EncodeTiledFn enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -125,7 +131,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   CUresult r = enc(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                    2, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    stream_hint ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
                                : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -371,6 +378,51 @@ static int up_project_impl(const mla_decode_dims* d, const void* w_uv, const uin
                                    w8, w8_scale, one_wave));
 }
 
+// Whether a whole run takes the up-projection that also corrects the lse of
+// unsplit sequences (then the combine merges split sequences only): 128
+// tokens or more, in more (128-token tile, head) units than there are SMs.
+// Measured: 512 tokens x 128 heads (512 units), step 319.3 -> 314.8 us; 128
+// tokens x 128 heads (128 units on 152 SMs, one per SM), 235.4 -> 236.8 us.
+static int run_uses_up_rows(const mla_decode_dims* d, bool* rows) {
+  int sms = 0;
+  const int rc = sm_count(&sms);
+  if (rc) return rc;
+  const int BT = d->batch * d->q_len;
+  *rows = BT >= 128 && static_cast<int64_t>((BT + 127) / 128) * d->num_heads > sms;
+  return MLA_DECODE_OK;
+}
+
+// The up-projection of such a run: untransposed, and it also adds the
+// first-order LSE correction to the rows of unsplit sequences.  bf16 weights
+// (w_uv) or FP8 weights (w8 with block scales).
+static int up_project_rows_impl(const mla_decode_dims* d, const void* w_uv, const uint8_t* w8,
+                                const float* w8_scale, float scale, void* out, float* lse,
+                                void* ws, size_t ws_bytes, void* stream) {
+  WsLayout L;
+  int rc = layout_for(d, ws_bytes, &L);
+  if (rc) return rc;
+  const int BT = d->batch * d->q_len, H = d->num_heads;
+  CUtensorMap tm_w, tm_o, tm_q, tm_out;
+  if (!(w8 ? make_map(&tm_w, w8, static_cast<uint64_t>(H) * kLora, kVHead, kVHead, 128, 64,
+                      false, 1)
+           : make_map(&tm_w, w_uv, static_cast<uint64_t>(H) * kLora, kVHead, kVHead, kBoxCols,
+                      64, false)) ||
+      !make_map(&tm_o, at<void>(ws, L.olat), BT, static_cast<uint64_t>(H) * kLora,
+                static_cast<uint64_t>(H) * kLora, kBoxCols, 128, false) ||
+      !make_map(&tm_q, at<void>(ws, L.qlo), BT, static_cast<uint64_t>(H) * kLora,
+                static_cast<uint64_t>(H) * kLora, 64, 128, false, 1, false) ||
+      !make_map(&tm_out, out, BT, static_cast<uint64_t>(H) * kVHead,
+                static_cast<uint64_t>(H) * kVHead, kBoxCols, 128, false))
+    return MLA_DECODE_CUDA_ERROR;
+  int sms = 0;
+  rc = sm_count(&sms);
+  if (rc) return rc;
+  return cuda_rc(launch_up_project_rows(tm_w, tm_o, tm_q, tm_out, BT, d->q_len, H,
+                                        at<int32_t>(ws, L.seq_nsplit), lse, scale,
+                                        at<int32_t>(ws, L.status), w8 ? w8_scale : nullptr, sms,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 int mla_decode_absorb(const mla_decode_dims* d, const void* q, const void* w_uk, void* ws,
                       size_t ws_bytes, void* stream) {
   if (!w_uk) return MLA_DECODE_INVALID_ARG;
@@ -415,8 +467,10 @@ int mla_decode_attend(const mla_decode_dims* d, const void* kv_cache, const int3
       d->num_pages, scale, static_cast<cudaStream_t>(stream)));
 }
 
-int mla_decode_combine(const mla_decode_dims* d, float scale, float* lse, void* ws,
-                       size_t ws_bytes, void* stream) {
+// split_only: leave the rows of unsplit sequences alone (their LSE correction
+// is then the up-projection's; see up_project_rows_impl).
+static int combine_impl(const mla_decode_dims* d, float scale, float* lse, void* ws,
+                        size_t ws_bytes, void* stream, bool split_only) {
   int rc = check_dims(d);
   if (rc) return rc;
   if (!softmax_scale_ok(scale) || !lse || !ws || !aligned16(ws) ||
@@ -436,7 +490,13 @@ int mla_decode_combine(const mla_decode_dims* d, float scale, float* lse, void* 
                                 at<PlanHeader>(ws, L.header), at<uint8_t>(ws, L.qlo),
                                 at<__nv_bfloat16>(ws, L.olat), lse, d->batch, d->q_len,
                                 d->num_heads, scale, splits_per_seq,
+                                split_only ? (ranges > 1 ? ranges - 1 : 1) : 0,
                                 static_cast<cudaStream_t>(stream)));
+}
+
+int mla_decode_combine(const mla_decode_dims* d, float scale, float* lse, void* ws,
+                       size_t ws_bytes, void* stream) {
+  return combine_impl(d, scale, lse, ws, ws_bytes, stream, false);
 }
 
 int mla_decode_up_project(const mla_decode_dims* d, const void* w_uv, void* out, void* ws,
@@ -478,8 +538,17 @@ int mla_decode_run(const mla_decode_dims* d, const void* q, const void* kv_cache
   if (rc) return rc;
   rc = mla_decode_attend(d, kv_cache, block_table, seq_lens, scale, lse, ws, ws_bytes, stream);
   if (rc) return rc;
-  rc = mla_decode_combine(d, scale, lse, ws, ws_bytes, stream);
+  // Large batches: the combine merges split sequences only and the
+  // up-projection corrects the lse of the others from the o_lat and q_lo
+  // tiles it stages anyway (one read of each instead of two).
+  bool rows = false;
+  rc = run_uses_up_rows(d, &rows);
   if (rc) return rc;
+  rc = combine_impl(d, scale, lse, ws, ws_bytes, stream, rows);
+  if (rc) return rc;
+  if (rows)
+    return up_project_rows_impl(d, w_uv, nullptr, nullptr, scale, out, lse, ws, ws_bytes,
+                                stream);
   return mla_decode_up_project(d, w_uv, out, ws, ws_bytes, stream);
 }
 
@@ -495,8 +564,14 @@ int mla_decode_run_fp8w(const mla_decode_dims* d, const void* q, const void* kv_
   if (rc) return rc;
   rc = mla_decode_attend(d, kv_cache, block_table, seq_lens, scale, lse, ws, ws_bytes, stream);
   if (rc) return rc;
-  rc = mla_decode_combine(d, scale, lse, ws, ws_bytes, stream);
+  bool rows = false;  // as in mla_decode_run
+  rc = run_uses_up_rows(d, &rows);
   if (rc) return rc;
+  rc = combine_impl(d, scale, lse, ws, ws_bytes, stream, rows);
+  if (rc) return rc;
+  if (rows)
+    return up_project_rows_impl(d, nullptr, w_uv_fp8, w_uv_scale, scale, out, lse, ws, ws_bytes,
+                                stream);
   return mla_decode_up_project_fp8w(d, w_uv_fp8, w_uv_scale, out, ws, ws_bytes, stream);
 }
 

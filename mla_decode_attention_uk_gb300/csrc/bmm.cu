@@ -100,6 +100,13 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
+// Two E4M3 values (the low 16 bits of `bits`, first value in the low byte) of
+// the scaled residual q_lo * 2^10, widened exactly to fp32.
+__device__ __forceinline__ float2 qlo_pair(uint32_t bits) {
+  const __nv_fp8x2_storage_t pr = static_cast<__nv_fp8x2_storage_t>(bits & 0xFFFFu);
+  return __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
+}
+
 // One converter thread's share of a raw FP8 weight tile: k row kr, m (or n)
 // columns 64 half .. 64 half + 63.  The raw tile arrives by TMA with 128B
 // swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)); the bf16 tile is
@@ -715,6 +722,323 @@ absorb_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_consta
   griddep_wait();
 }
 
+// Up-projection for 128 tokens or more (bf16 weights), with the first-order
+// LSE correction of the rows of unsplit sequences folded in: the combine step
+// then visits only split sequences' rows (merging their partials and
+// correcting their lse), where it would otherwise re-read o_lat and q_lo of
+// every row.  The product runs untransposed, D[tok, m] = sum_k
+// o_lat[tok, h, k] W_UV[h][k][m], one unit per (128-token tile, head): M = 128
+// tokens, N = 128, K = 512 in eight 64-deep stages.  Each stage brings by TMA
+// the o_lat tile (A, K-major), a 64-row slice of W_UV[h] (B, MN-major: two
+// 64-column boxes) and the q_lo tile of the same rows and columns (64 E4M3
+// bytes per row), so the correction warps dot o with q_lo out of shared
+// memory while the tensor core consumes the same stage; the stage is
+// released once both are done with it.  Persistent: one CTA per SM walks the
+// units.
+//   warp 0: TMA producer; warp 1: TMEM owner and MMA issuer; warps 2-9:
+//   correction (thread ct: token row ct % 128, column half ct / 128 of each
+//   stage); warps 10-13: epilogue (TMEM lane quarter = warp % 4), out through
+//   a 128B-swizzled staging tile and TMA tensor stores.
+//
+// FP8 weights (W8): each stage brings the raw 64 k x 128 m FP8 slice instead,
+// and warps 14-17 decompress it into the B operand (convert_fp8_row: the same
+// layout as the transposed kernel's bf16 weight tile); three stages.
+constexpr int kUrCorrThreads = 256;
+constexpr int kUrABytes = 128 * 128;                 // 128 tokens x 64 k, bf16
+constexpr int kUrBBytes = 2 * kBoxBytes;             // 64 k x 128 m, bf16
+constexpr int kUrQBytes = 128 * 64;                  // 128 tokens x 64 k, E4M3
+constexpr int kUrOutBytes = 2 * 128 * 128;           // 128 tokens x 128 m, bf16
+template <bool W8>
+struct UpRowsCfg {
+  static constexpr int kThreads = 64 + kUrCorrThreads + 128 + (W8 ? 128 : 0);
+  static constexpr int kStages = W8 ? 3 : 4;
+  static constexpr int kRawStage = W8 ? kRawBytes : 0;   // raw FP8 slice (W8)
+  static constexpr int kStageBytes = kUrABytes + kUrBBytes + kUrQBytes + kRawStage;  // 40 / 48 KB
+  // TMA bytes per stage: the B operand arrives raw (W8) or as bf16.
+  static constexpr int kTxBytes = kUrABytes + kUrQBytes + (W8 ? kRawBytes : kUrBBytes);
+  // One staging buffer: with two, dynamic and static shared memory would pass
+  // the 227 KB a CTA may have.
+  static constexpr int kSmem = kStages * kStageBytes + kUrOutBytes + 1024;
+};
+
+template <bool W8>
+__global__ void __launch_bounds__(UpRowsCfg<W8>::kThreads, 1)
+up_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_o,
+               const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
+               int BT, int T, int H, const int32_t* __restrict__ seq_nsplit,
+               float* __restrict__ lse, float scale, int32_t* __restrict__ status,
+               const float* __restrict__ w8_scale) {
+  using C = UpRowsCfg<W8>;
+  constexpr int kUrStages = C::kStages;
+  constexpr int kUrStageBytes = C::kStageBytes;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kUrStages], empty_bar[kUrStages],
+      conv_bar[W8 ? kUrStages : 1], acc_full[2], acc_empty[2], drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  __shared__ float corr_sh[2][2][128];  // [unit parity][column half][row]
+
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntt = (BT + 127) / 128;
+  const int units = ntt * H;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sout = sbase + kUrStages * kUrStageBytes;
+  // Unit u: token tile u % ntt, head u / ntt.
+  constexpr int kNk = kLora / 64;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kUrStages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      // The MMA issuer's commit and one arrival per correction warp.
+      mbar_init(smem_u32(&empty_bar[s]), 1 + kUrCorrThreads / 32);
+      if constexpr (W8) mbar_init(smem_u32(&conv_bar[s]), 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(smem_u32(&acc_full[j]), 1);
+      mbar_init(smem_u32(&acc_empty[j]), 4);
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
+    abort_sh = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_o);
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_out);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  // The stage's slice of W_UV: two bf16 boxes into the B operand, or the raw
+  // FP8 slice (W8) next to the stage's other tiles.
+  auto load_w = [&](uint32_t st, int h, int kc, uint32_t fb) {
+    if constexpr (W8) {
+      tma_load_2d(st + kUrABytes + kUrBBytes + kUrQBytes, &tm_w, 0, h * kLora + kc * 64, fb);
+    } else {
+      tma_load_2d(st + kUrABytes, &tm_w, 0, h * kLora + kc * 64, fb);
+      tma_load_2d(st + kUrABytes + kBoxBytes, &tm_w, 64, h * kLora + kc * 64, fb);
+    }
+  };
+  if (warp == 0) {
+    if (elect_one()) {
+      // The weight slices of the first stages do not depend on the previous
+      // step: they load before the wait for it, o_lat and q_lo after.
+      const int u0 = blockIdx.x;
+      const int first = u0 < units ? (kNk < kUrStages ? kNk : kUrStages) : 0;
+      for (int kc = 0; kc < first; ++kc) {
+        const uint32_t st = sbase + kc * kUrStageBytes;
+        const uint32_t fb = smem_u32(&full_bar[kc]);
+        const int h = u0 / ntt;
+        mbar_expect_tx(fb, C::kTxBytes);
+        load_w(st, h, kc, fb);
+      }
+      griddep_wait();  // o_lat and q_lo come from the steps before
+      int g = 0;
+      bool ok = true;
+      for (int u = u0; u < units && ok; u += gridDim.x) {
+        const int tok0 = (u % ntt) * 128, h = u / ntt;
+        for (int kc = 0; kc < kNk; ++kc, ++g) {
+          const int s = g % kUrStages;
+          const uint32_t st = sbase + s * kUrStageBytes;
+          const uint32_t fb = smem_u32(&full_bar[s]);
+          if (g >= first) {
+            if (g >= kUrStages &&
+                !mbar_wait(smem_u32(&empty_bar[s]), ((g / kUrStages) - 1) & 1, &abort_sh,
+                           status)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(fb, C::kTxBytes);
+            load_w(st, h, kc, fb);
+          }
+          tma_load_2d(st, &tm_o, h * kLora + kc * 64, tok0, fb);
+          tma_load_2d(st + kUrABytes + kUrBBytes, &tm_q, h * kLora + kc * 64, tok0, fb);
+        }
+      }
+      // Copies still in flight (only after a timeout) land before the CTA
+      // exits: wait for the last load of each stage.
+      for (int j = g > kUrStages ? g - kUrStages : 0; j < g; ++j)
+        mbar_wait_drain(smem_u32(&full_bar[j % kUrStages]), (j / kUrStages) & 1, status);
+    }
+  } else if (warp == 1) {
+    griddep_wait();
+    if (elect_one()) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128, /*a_mn=*/false, /*b_mn=*/true);
+      int g = 0, i = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
+        const int j = i & 1;
+        if (i >= 2 &&
+            !mbar_wait(smem_u32(&acc_empty[j]), ((i >> 1) - 1) & 1, &abort_sh, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kc = 0; kc < kNk; ++kc, ++g) {
+          const int s = g % kUrStages;
+          if (!mbar_wait(smem_u32(&full_bar[s]), (g / kUrStages) & 1, &abort_sh, status) ||
+              (W8 && !mbar_wait(smem_u32(&conv_bar[s]), (g / kUrStages) & 1, &abort_sh, status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = sbase + s * kUrStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sdesc_sw128(st + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(st + kUrABytes + kk * 2048, kBoxBytes, 1024);
+            umma_bf16(tmem + 128 * j, ad, bd, idesc, (kc | kk) != 0);
+          }
+          umma_commit(smem_u32(&empty_bar[s]));
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&acc_full[j]));
+      }
+      umma_commit(smem_u32(&drain_bar));
+      mbar_wait_drain(smem_u32(&drain_bar), 0, status);
+    }
+  } else if (warp < 2 + kUrCorrThreads / 32) {
+    // Correction warps: thread ct owns token row r = ct % 128 of each unit
+    // and columns 32 hf .. 32 hf + 31 (hf = ct / 128) of each 64-column
+    // stage: 64 bytes of o (A rows are 128 bytes, 16-byte chunk c at
+    // c ^ (r & 7)) and 32 bytes of q_lo (64-byte rows, unswizzled).
+    griddep_wait();
+    const int ct = threadIdx.x - 64;
+    const int r = ct & 127, hf = ct >> 7;
+    int g = 0, i = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++i) {
+      const int tok0 = (u % ntt) * 128, h = u / ntt;
+      const int tok = tok0 + r;
+      const bool mine = tok < BT && seq_nsplit[tok / T] <= 1;  // unsplit rows only
+      float corr = 0.0f;
+      for (int kc = 0; kc < kNk; ++kc, ++g) {
+        const int s = g % kUrStages;
+        ok = mbar_wait(smem_u32(&full_bar[s]), (g / kUrStages) & 1, &abort_sh, status);
+        if (!ok) break;
+        if (mine) {
+          const uint32_t st = sbase + s * kUrStageBytes;
+          const uint32_t arow = st + r * 128;
+          const uint32_t qrow = st + kUrABytes + kUrBBytes + r * 64 + hf * 32;
+          const uint4 q0 = ld_shared_v4(qrow), q1 = ld_shared_v4(qrow + 16);
+          const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 ov = ld_shared_v4(arow + (((4 * hf + c) ^ (r & 7)) << 4));
+            const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(&ow[e]);
+              const float2 l2 = qlo_pair(qw[2 * c + (e >> 1)] >> (16 * (e & 1)));
+              corr += l2.x * __low2float(o2) + l2.y * __high2float(o2);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
+      }
+      // The two column halves of a row meet in shared memory (one buffer per
+      // unit parity, so one barrier per unit suffices).
+      corr_sh[i & 1][hf][r] = corr;
+      if (!named_bar_and(1, kUrCorrThreads, ok)) break;
+      if (hf == 0 && mine) {
+        const size_t row = static_cast<size_t>(tok) * H + h;
+        lse[row] += scale * kQloInvScale * (corr_sh[i & 1][0][r] + corr_sh[i & 1][1][r]);
+      }
+    }
+  } else if (W8 && warp >= 2 + kUrCorrThreads / 32 + 4) {
+    // FP8 converters (warps 14-17): thread ct owns k row ct / 2, columns
+    // 64 (ct % 2) .. + 63 of each stage's weight slice.
+    griddep_wait();
+    const int ct = threadIdx.x - 64 - kUrCorrThreads - 128;
+    int g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const int h = u / ntt;
+      for (int kc = 0; kc < kNk; ++kc, ++g) {
+        const int s = g % kUrStages;
+        ok = mbar_wait(smem_u32(&full_bar[s]), (g / kUrStages) & 1, &abort_sh, status);
+        if (!named_bar_and(3, 128, ok)) {
+          ok = false;
+          break;
+        }
+        // W_UV scales [H, 4, 1]: one per 128 k rows.
+        const float sc = __ldg(w8_scale + h * (kLora / 128) + kc / 2);
+        const uint32_t st = sbase + s * kUrStageBytes;
+        convert_fp8_row(st + kUrABytes + kUrBBytes + kUrQBytes, st + kUrABytes, ct >> 1, ct & 1,
+                        sc);
+        fence_proxy_async_smem();  // the bf16 slice goes to the tensor core
+        named_bar_sync(3, 128);
+        if (ct == 0) mbar_arrive(smem_u32(&conv_bar[s]));
+      }
+    }
+  } else {
+    // Epilogue: thread (quarter q4 = warp % 4, lane) owns token row
+    // 32 q4 + lane of each unit (TMEM lane); out goes to the staging buffer
+    // (two 64-column boxes, 128-byte rows, 16-byte chunk c at c ^ (row & 7))
+    // and out by two tensor stores.
+    griddep_wait();
+    const int q4 = warp & 3;
+    const int rr = q4 * 32 + lane;
+    const int et = threadIdx.x - 64 - kUrCorrThreads;  // 0..127
+    const uint32_t rsw = static_cast<uint32_t>(rr & 7);
+    int i = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++i) {
+      const int tok0 = (u % ntt) * 128, h = u / ntt;
+      const int j = i & 1;
+      const uint32_t ot = sout;
+      const bool ok = mbar_wait(smem_u32(&acc_full[j]), (i >> 1) & 1, &abort_sh, status);
+      // The staging buffer was last read by the tensor stores of unit i - 1.
+      if (et == 0) tma_store_wait_read();
+      if (!named_bar_and(2, 128, ok)) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem + 128 * j + (static_cast<uint32_t>(q4 * 32) << 16) + c * 32, v);
+        tmem_wait_ld();
+        uint32_t hw[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const __nv_bfloat162 hv =
+              __floats2bfloat162_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+          hw[e] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        const uint32_t orow = ot + (c >> 1) * (128 * 128) + rr * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          st_shared_v4(orow + (((4 * (c & 1) + k) ^ rsw) << 4), hw[4 * k], hw[4 * k + 1],
+                       hw[4 * k + 2], hw[4 * k + 3]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[j]));
+      fence_proxy_async_smem();
+      named_bar_sync(2, 128);
+      if (et == 0) {
+        tma_store_2d(&tm_out, h * kVHead, tok0, ot);
+        tma_store_2d(&tm_out, h * kVHead + 64, tok0, ot + 128 * 128);
+        tma_store_commit();
+      }
+    }
+    if (et == 0) tma_store_wait_read();
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+
 template <BmmMode MODE, int NT, int kStagesAll = 0>
 cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, int H, int K,
                           int Kx, int Mtot, const __nv_bfloat16* q, __nv_bfloat16* hi,
@@ -750,6 +1074,23 @@ cudaError_t launch_absorb_rows(const CUtensorMap& tw, const CUtensorMap& tx,
   e = launch_pdl(absorb_rows_kernel<W8>, dim3(units < sm_count ? units : sm_count),
                  dim3(C::kThreads), C::kSmem, st, tw, tx, thi, tlo, BT, H, q, hi, status,
                  w8_scale);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <bool W8>
+cudaError_t launch_up_rows(const CUtensorMap& tw, const CUtensorMap& to, const CUtensorMap& tq,
+                           const CUtensorMap& tout, int BT, int T, int H,
+                           const int32_t* seq_nsplit, float* lse, float scale, int32_t* status,
+                           const float* w8_scale, int sm_count, cudaStream_t st) {
+  using C = UpRowsCfg<W8>;
+  cudaError_t e = cudaFuncSetAttribute(up_rows_kernel<W8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  const int units = (BT + 127) / 128 * H;
+  e = launch_pdl(up_rows_kernel<W8>, dim3(units < sm_count ? units : sm_count),
+                 dim3(C::kThreads), C::kSmem, st, tw, to, tq, tout, BT, T, H, seq_nsplit, lse,
+                 scale, status, w8_scale);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -816,6 +1157,17 @@ cudaError_t launch_up_project(const CUtensorMap& tm_wuv, const CUtensorMap& tm_o
     case 64: return launch_bmm_nt<BmmMode::kUpProject, 64>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);
     default: return launch_bmm_nt<BmmMode::kUpProject, 128>(tm_wuv, tm_olat, BT, H, kLora, kLora, kVHead, nullptr, out, nullptr, status, st, w8);
   }
+}
+
+cudaError_t launch_up_project_rows(const CUtensorMap& tm_wuv, const CUtensorMap& tm_olat,
+                                   const CUtensorMap& tm_qlo, const CUtensorMap& tm_out, int BT,
+                                   int T, int H, const int32_t* seq_nsplit, float* lse,
+                                   float scale, int32_t* status, const float* wuv_scale,
+                                   int sm_count, cudaStream_t st) {
+  return wuv_scale ? launch_up_rows<true>(tm_wuv, tm_olat, tm_qlo, tm_out, BT, T, H, seq_nsplit,
+                                          lse, scale, status, wuv_scale, sm_count, st)
+                   : launch_up_rows<false>(tm_wuv, tm_olat, tm_qlo, tm_out, BT, T, H, seq_nsplit,
+                                           lse, scale, status, nullptr, sm_count, st);
 }
 
 }  // namespace mla

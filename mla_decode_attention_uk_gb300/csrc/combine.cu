@@ -45,55 +45,18 @@ __device__ __forceinline__ float2 qlo_pair(uint32_t bits) {
 }
 constexpr int kRowsPerCta = kCombThreads / 32;
 
-// At least three CTAs per SM: the unrolled instantiations then get up to 85
-// registers and do not spill (left to itself ptxas picks 64 and spills).
+// One warp merges row r of split sequence b (ns splits, partial slots from
+// slot0): lse and o over the splits, o_lat as bf16, and the lse with its
+// first-order correction.
 template <int kUnroll, bool kFew>
-__global__ void __launch_bounds__(kCombThreads, 3)
-combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict__ seq_slot,
-               const uint8_t* __restrict__ ws, const PlanHeader* __restrict__ header, int B,
-               int T, int H, const uint8_t* __restrict__ qlo,
-               __nv_bfloat16* __restrict__ olat, float* __restrict__ lse_out, float scale) {
-  // The plan and q_lo are complete when this kernel starts (the attention
-  // step waited for them before letting it launch), so they are read before
-  // waiting for the attention step itself.
-  griddep_launch_dependents();
+__device__ __forceinline__ void merge_split_row(int b, int r, int lane, int ns, int slot0, int B,
+                                                int T, int H, const uint8_t* __restrict__ ws,
+                                                const PlanHeader* __restrict__ header,
+                                                const uint8_t* __restrict__ qlo,
+                                                __nv_bfloat16* __restrict__ olat,
+                                                float* __restrict__ lse_out, float scale) {
   const int TH = T * H;
-  const int b = blockIdx.y;
-  const int r = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= TH) {
-    griddep_wait();
-    return;
-  }
-  const int ns = seq_nsplit[b];
   const size_t row = static_cast<size_t>(b) * TH + r;
-  if (ns <= 1) {
-    // Unsplit: o_lat and lse were written by the attention step.
-    const uint4* o4 = reinterpret_cast<const uint4*>(olat + row * kLora) + lane * 2;
-    // This lane's 16 latent columns of q_lo: 16 E4M3 bytes.
-    const uint4 lv = *(reinterpret_cast<const uint4*>(qlo + row * kLora) + lane);
-    griddep_wait();
-    // The row's lse goes out with the o_lat loads: one round trip, not two.
-    const float lse_in = lane == 0 ? lse_out[row] : 0.0f;
-    float corr = 0.0f;
-    const uint32_t lw[4] = {lv.x, lv.y, lv.z, lv.w};
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const uint4 ov = o4[q];
-      const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(&ow[e]);
-        const float2 l2 = qlo_pair(lw[2 * q + (e >> 1)] >> (16 * (e & 1)));
-        corr += l2.x * __low2float(o2) + l2.y * __high2float(o2);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) corr += __shfl_xor_sync(0xffffffffu, corr, o);
-    if (lane == 0) lse_out[row] = lse_in + scale * kQloInvScale * corr;
-    return;
-  }
-  const int slot0 = seq_slot[b];
   uint32_t lo_raw[4];  // 4 E4M3 residuals per (q, lane): columns (32 q + lane) * 4 ..
 #pragma unroll
   for (int q = 0; q < 4; ++q)
@@ -201,16 +164,108 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
   if (lane == 0) lse_out[row] = lse + scale * kQloInvScale * corr;
 }
 
+// At least three CTAs per SM: the unrolled instantiations then get up to 85
+// registers and do not spill (left to itself ptxas picks 64 and spills).
+template <int kUnroll, bool kFew>
+__global__ void __launch_bounds__(kCombThreads, 3)
+combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict__ seq_slot,
+               const uint8_t* __restrict__ ws, const PlanHeader* __restrict__ header, int B,
+               int T, int H, const uint8_t* __restrict__ qlo,
+               __nv_bfloat16* __restrict__ olat, float* __restrict__ lse_out, float scale) {
+  // The plan and q_lo are complete when this kernel starts (the attention
+  // step waited for them before letting it launch), so they are read before
+  // waiting for the attention step itself.
+  griddep_launch_dependents();
+  const int TH = T * H;
+  const int b = blockIdx.y;
+  const int r = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= TH) {
+    griddep_wait();
+    return;
+  }
+  const int ns = seq_nsplit[b];
+  const size_t row = static_cast<size_t>(b) * TH + r;
+  if (ns <= 1) {
+    // Unsplit: o_lat and lse were written by the attention step.
+    const uint4* o4 = reinterpret_cast<const uint4*>(olat + row * kLora) + lane * 2;
+    // This lane's 16 latent columns of q_lo: 16 E4M3 bytes.
+    const uint4 lv = *(reinterpret_cast<const uint4*>(qlo + row * kLora) + lane);
+    griddep_wait();
+    // The row's lse goes out with the o_lat loads: one round trip, not two.
+    const float lse_in = lane == 0 ? lse_out[row] : 0.0f;
+    float corr = 0.0f;
+    const uint32_t lw[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint4 ov = o4[q];
+      const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(&ow[e]);
+        const float2 l2 = qlo_pair(lw[2 * q + (e >> 1)] >> (16 * (e & 1)));
+        corr += l2.x * __low2float(o2) + l2.y * __high2float(o2);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) corr += __shfl_xor_sync(0xffffffffu, corr, o);
+    if (lane == 0) lse_out[row] = lse_in + scale * kQloInvScale * corr;
+    return;
+  }
+  merge_split_row<kUnroll, kFew>(b, r, lane, ns, seq_slot[b], B, T, H, ws, header, qlo, olat,
+                                 lse_out, scale);
+}
+
+// Split sequences only, for a run whose up-projection corrects the lse of the
+// unsplit rows itself.  Sequence b is split exactly when a work range starts
+// inside it, and the first such range is k = seq_first[b] + 1, so walking the
+// ranges visits every split sequence once; the grid's y dimension strides
+// over them.  (A kernel of its own: the loop around the merge would cost the
+// other instantiations registers; its grid is small, so two CTAs per SM with
+// up to 128 registers are enough.)
+template <int kUnroll, bool kFew>
+__global__ void __launch_bounds__(kCombThreads, 2)
+combine_split_kernel(const int32_t* __restrict__ seq_nsplit,
+                     const int32_t* __restrict__ seq_slot, const uint8_t* __restrict__ ws,
+                     const PlanHeader* __restrict__ header, int B, int T, int H,
+                     const uint8_t* __restrict__ qlo, __nv_bfloat16* __restrict__ olat,
+                     float* __restrict__ lse_out, float scale) {
+  // The plan is complete when this kernel starts (as in combine_kernel).
+  griddep_launch_dependents();
+  const int TH = T * H;
+  const int r = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r < TH) {
+    const WsLayout L = make_layout(B, T, H, header->num_ranges);
+    const int32_t* __restrict__ range_b = reinterpret_cast<const int32_t*>(ws + L.range_b);
+    const int32_t* __restrict__ range_p = reinterpret_cast<const int32_t*>(ws + L.range_p);
+    const int32_t* __restrict__ seq_first = reinterpret_cast<const int32_t*>(ws + L.seq_first);
+    for (int k = blockIdx.y + 1; k < L.num_ranges; k += gridDim.y) {
+      const int b = range_b[k];
+      if (b >= B || range_p[k] == 0 || seq_first[b] + 1 != k) continue;
+      merge_split_row<kUnroll, kFew>(b, r, lane, seq_nsplit[b], seq_slot[b], B, T, H, ws,
+                                     header, qlo, olat, lse_out, scale);
+    }
+  }
+  griddep_wait();
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, const void* ws,
                            const PlanHeader* header, const uint8_t* qlo,
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
-                           int splits_per_seq, cudaStream_t st) {
-  dim3 grid((T * H + kRowsPerCta - 1) / kRowsPerCta, B);
+                           int splits_per_seq, int split_ranges, cudaStream_t st) {
+  // split_ranges > 0: split sequences only, the grid's y dimension striding
+  // over that many work ranges (the planner's count or any other).
+  const bool split_only = split_ranges > 0;
+  dim3 grid((T * H + kRowsPerCta - 1) / kRowsPerCta, split_only ? split_ranges : B);
   // splits_per_seq: work ranges per sequence, rounded up (the host's guess of
-  // the typical split count; only the speed depends on it).
-  auto kern = splits_per_seq <= 1   ? combine_kernel<1, false>
+  // the typical split count; only the speed depends on it).  Split-only
+  // launches take the unrolled split loop (its few-splits path would spill
+  // there).
+  auto kern = split_only ? combine_split_kernel<4, false>
+              : splits_per_seq <= 1 ? combine_kernel<1, false>
               : splits_per_seq <= 4 ? combine_kernel<4, true>
                                     : combine_kernel<4, false>;
   cudaError_t e = launch_pdl(kern, grid, dim3(kCombThreads), 0, st, seq_nsplit, seq_slot,
