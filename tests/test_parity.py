@@ -193,6 +193,38 @@ def test_step_calls_equal_run_bitwise():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("R", [0, 400])
+def test_large_run_matches_step_calls(R):
+    # 160 tokens x 128 heads: 256 (128-token tile, head) units, more than the
+    # SMs, so mla_decode_run merges split sequences only in the combine and
+    # corrects the other rows in its up-projection, while the step calls keep
+    # the combine for every row.  out must agree bit for bit (same o_lat, same
+    # products), lse up to the summation order of the correction; both match
+    # the oracle on every row.  R = 400 ranges (default: one per SM group)
+    # cuts sequences into many splits and makes the split-only combine's grid
+    # stride over more ranges than it was sized for.
+    g = torch.Generator().manual_seed(91 + R)
+    lens = torch.randint(1, 2500, (160,), generator=g).tolist()
+    inp = make_inputs(160, lens, 1, 128, seed=92)
+    dev = torch.device("cuda")
+    gd = inp.to(dev)
+    m = binding.MlaDecode(binding.dims_for(gd.q, gd.cache, gd.block_table), dev, R)
+    o1 = torch.empty(160, 1, 128, 128, dtype=torch.bfloat16, device=dev)
+    l1 = torch.empty(160, 1, 128, dtype=torch.float32, device=dev)
+    o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
+    m.plan(gd.seq_lens)
+    m.run(gd.q, gd.cache, gd.block_table, gd.seq_lens, gd.w_uk, gd.w_uv, gd.scale, o1, l1)
+    m.plan(gd.seq_lens)
+    m.absorb(gd.q, gd.w_uk)
+    m.attend(gd.cache, gd.block_table, gd.seq_lens, gd.scale, l2)
+    m.combine(gd.scale, l2)
+    m.up_project(gd.w_uv, o2)
+    assert m.check() == 0
+    assert torch.equal(o1, o2)
+    assert (l1 - l2).abs().max().item() <= 1e-6
+    assert_parity(compare(inp, o1.cpu(), l1.cpu()), "large run R=%d" % R)
+
+
 def test_page_permutation_same_schedule_bitwise():
     inp = make_inputs(3, [130, 640, 77], 1, 32, seed=10)
     o1, l1, _ = run_gpu(inp)
