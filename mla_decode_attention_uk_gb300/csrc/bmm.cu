@@ -917,6 +917,10 @@ up_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
       const int tok0 = (u % ntt) * 128, h = u / ntt;
       const int tok = tok0 + r;
       const bool mine = tok < BT && seq_nsplit[tok / T] <= 1;  // unsplit rows only
+      const size_t row = static_cast<size_t>(tok) * H + h;
+      // The row's lse (from the attention step) loads now, under the stages,
+      // rather than at the end of the unit where it would hold up the next.
+      const float lse_in = (mine && hf == 0) ? lse[row] : 0.0f;
       float corr = 0.0f;
       for (int kc = 0; kc < kNk; ++kc, ++g) {
         const int s = g % kUrStages;
@@ -947,10 +951,8 @@ up_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
       // unit parity, so one barrier per unit suffices).
       corr_sh[i & 1][hf][r] = corr;
       if (!named_bar_and(1, kUrCorrThreads, ok)) break;
-      if (hf == 0 && mine) {
-        const size_t row = static_cast<size_t>(tok) * H + h;
-        lse[row] += scale * kQloInvScale * (corr_sh[i & 1][0][r] + corr_sh[i & 1][1][r]);
-      }
+      if (hf == 0 && mine)
+        lse[row] = lse_in + scale * kQloInvScale * (corr_sh[i & 1][0][r] + corr_sh[i & 1][1][r]);
     }
   } else if (W8 && warp >= 2 + kUrCorrThreads / 32 + 4) {
     // FP8 converters (warps 14-17): thread ct owns k row ct / 2, columns
