@@ -48,7 +48,7 @@ constexpr int kRowsPerCta = kCombThreads / 32;
 // One warp merges row r of split sequence b (ns splits, partial slots from
 // slot0): lse and o over the splits, o_lat as bf16, and the lse with its
 // first-order correction.
-template <int kUnroll, bool kFew>
+template <int kUnroll, int kFewN>
 __device__ __forceinline__ void merge_split_row(int b, int r, int lane, int ns, int slot0, int B,
                                                 int T, int H, const uint8_t* __restrict__ ws,
                                                 const PlanHeader* __restrict__ header,
@@ -70,12 +70,14 @@ __device__ __forceinline__ void merge_split_row(int b, int r, int lane, int ns, 
 #pragma unroll
   for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
   float lse;
-  if (kFew && ns <= 4) {
-    // Every split's lse and partial output go out at once.
-    float l[4];
-    float4 v[4][4];
+  if (kFewN > 0 && ns <= kFewN) {
+    // Every split's lse and partial output go out at once (one memory round
+    // trip instead of one per split).
+    constexpr int kN = kFewN > 0 ? kFewN : 1;
+    float l[kN];
+    float4 v[kN][4];
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
+    for (int s = 0; s < kN; ++s) {
       l[s] = -INFINITY;
       if (s < ns) {
         const size_t srow = static_cast<size_t>(slot0 + s) * TH + r;
@@ -85,13 +87,15 @@ __device__ __forceinline__ void merge_split_row(int b, int r, int lane, int ns, 
         for (int q = 0; q < 4; ++q) v[s][q] = src[q * 32 + lane];
       }
     }
-    const float m = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
+    float m = l[0];
+#pragma unroll
+    for (int s = 1; s < kN; ++s) m = fmaxf(m, l[s]);
     float wsum = 0.0f;
 #pragma unroll
-    for (int s = 0; s < 4; ++s) wsum += (l[s] == -INFINITY) ? 0.0f : __expf(l[s] - m);
+    for (int s = 0; s < kN; ++s) wsum += (l[s] == -INFINITY) ? 0.0f : __expf(l[s] - m);
     lse = m + __logf(wsum);
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
+    for (int s = 0; s < kN; ++s) {
       if (s < ns) {
         const float w = (l[s] == -INFINITY) ? 0.0f : __expf(l[s] - lse);
 #pragma unroll
@@ -166,7 +170,7 @@ __device__ __forceinline__ void merge_split_row(int b, int r, int lane, int ns, 
 
 // At least three CTAs per SM: the unrolled instantiations then get up to 85
 // registers and do not spill (left to itself ptxas picks 64 and spills).
-template <int kUnroll, bool kFew>
+template <int kUnroll, int kFewN>
 __global__ void __launch_bounds__(kCombThreads, 3)
 combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict__ seq_slot,
                const uint8_t* __restrict__ ws, const PlanHeader* __restrict__ header, int B,
@@ -212,7 +216,7 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
     if (lane == 0) lse_out[row] = lse_in + scale * kQloInvScale * corr;
     return;
   }
-  merge_split_row<kUnroll, kFew>(b, r, lane, ns, seq_slot[b], B, T, H, ws, header, qlo, olat,
+  merge_split_row<kUnroll, kFewN>(b, r, lane, ns, seq_slot[b], B, T, H, ws, header, qlo, olat,
                                  lse_out, scale);
 }
 
@@ -221,10 +225,10 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
 // inside it, and the first such range is k = seq_first[b] + 1, so walking the
 // ranges visits every split sequence once; the grid's y dimension strides
 // over them.  (A kernel of its own: the loop around the merge would cost the
-// other instantiations registers; its grid is small, so two CTAs per SM with
-// up to 128 registers are enough.)
-template <int kUnroll, bool kFew>
-__global__ void __launch_bounds__(kCombThreads, 2)
+// other instantiations registers; its grid is small, so it may use as many
+// as it needs.)
+template <int kUnroll, int kFewN>
+__global__ void __launch_bounds__(kCombThreads, 1)
 combine_split_kernel(const int32_t* __restrict__ seq_nsplit,
                      const int32_t* __restrict__ seq_slot, const uint8_t* __restrict__ ws,
                      const PlanHeader* __restrict__ header, int B, int T, int H,
@@ -243,7 +247,7 @@ combine_split_kernel(const int32_t* __restrict__ seq_nsplit,
     for (int k = blockIdx.y + 1; k < L.num_ranges; k += gridDim.y) {
       const int b = range_b[k];
       if (b >= B || range_p[k] == 0 || seq_first[b] + 1 != k) continue;
-      merge_split_row<kUnroll, kFew>(b, r, lane, seq_nsplit[b], seq_slot[b], B, T, H, ws,
+      merge_split_row<kUnroll, kFewN>(b, r, lane, seq_nsplit[b], seq_slot[b], B, T, H, ws,
                                      header, qlo, olat, lse_out, scale);
     }
   }
@@ -261,13 +265,14 @@ cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, c
   const bool split_only = split_ranges > 0;
   dim3 grid((T * H + kRowsPerCta - 1) / kRowsPerCta, split_only ? split_ranges : B);
   // splits_per_seq: work ranges per sequence, rounded up (the host's guess of
-  // the typical split count; only the speed depends on it).  Split-only
-  // launches take the unrolled split loop (its few-splits path would spill
-  // there).
-  auto kern = split_only ? combine_split_kernel<4, false>
-              : splits_per_seq <= 1 ? combine_kernel<1, false>
-              : splits_per_seq <= 4 ? combine_kernel<4, true>
-                                    : combine_kernel<4, false>;
+  // the typical split count; only the speed depends on it).  A split-only
+  // launch takes the same variant as the full combine would, so a split
+  // row's o_lat is the same bit for bit either way.
+  auto kern = splits_per_seq <= 1
+                  ? (split_only ? combine_split_kernel<1, 2> : combine_kernel<1, 2>)
+              : splits_per_seq <= 4
+                  ? (split_only ? combine_split_kernel<4, 4> : combine_kernel<4, 4>)
+                  : (split_only ? combine_split_kernel<4, 0> : combine_kernel<4, 0>);
   cudaError_t e = launch_pdl(kern, grid, dim3(kCombThreads), 0, st, seq_nsplit, seq_slot,
                              static_cast<const uint8_t*>(ws), header, B, T, H, qlo, olat, lse,
                              scale);
