@@ -470,9 +470,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // deep (two-input: 31, six deep).
             float a3[11];
 #pragma unroll
-            for (int i = 0; i < 10; ++i)
-              a3[i] = fmax3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]),
-                            __uint_as_float(v[3 * i + 2]));
+            for (int t3 = 0; t3 < 10; ++t3)
+              a3[t3] = fmax3(__uint_as_float(v[3 * t3]), __uint_as_float(v[3 * t3 + 1]),
+                             __uint_as_float(v[3 * t3 + 2]));
             a3[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
             const float b0 = fmax3(a3[0], a3[1], a3[2]), b1 = fmax3(a3[3], a3[4], a3[5]),
                         b2 = fmax3(a3[6], a3[7], a3[8]), b3 = fmaxf(a3[9], a3[10]);
