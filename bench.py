@@ -491,6 +491,7 @@ def main():
     hbm, bf16, bf16_sus, peak_src = measured_peaks()
 
     r = WorkloadRunner(args.workload, dev, fp8, use_graph=not args.no_graph)
+    launches_per_step = 1 + binding.kernels_per_run(r.m.dims, fp8)  # plan + the run's kernels
     stats, inp_cpu, g = r.stats, r.inp_cpu, r.g
     B, T, H = stats["B"], stats["T"], stats["H"]
     r.prepare(args.warmup)
@@ -632,7 +633,7 @@ def main():
         "e2e": {"value": world * stats["cache_bytes"] / e2e_s / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3},
-        "gpu_launches": args.steps * (1 + binding.lib().mla_decode_kernels_per_run()),
+        "gpu_launches": args.steps * launches_per_step,
         "launch_mode": ("cuda_graph, %d steps per replay" % per_graph) if per_graph > 1 else "host",
         "clocks": clocks.summary(),
     }

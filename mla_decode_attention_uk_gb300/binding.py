@@ -68,6 +68,7 @@ def lib():
         L.mla_decode_workspace_offsets.argtypes = [D, i32, ctypes.POINTER(ctypes.c_int64), i32]
         L.mla_decode_run_static_scratch.argtypes = [D, P, P, P, P, P, P, ctypes.c_float, P, P, P]
         L.mla_decode_selftest_wait_timeout.argtypes = [P, P]
+        L.mla_decode_kernels_per_run.argtypes = [D, i32, ctypes.POINTER(ctypes.c_int32)]
         L.mla_decode_run_fp8w.argtypes = [D, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, S, P]
         L.mla_decode_absorb_fp8w.argtypes = [D, P, P, P, P, S, P]
         L.mla_decode_up_project_fp8w.argtypes = [D, P, P, P, P, S, P]
@@ -109,6 +110,14 @@ def workspace_offsets(d: Dims, num_ranges: int = 0):
     _ok(lib().mla_decode_workspace_offsets(ctypes.byref(d), num_ranges, arr, 4),
         "mla_decode_workspace_offsets")
     return dict(qlat=arr[0], qlo=arr[1], olat=arr[2], header=arr[3])
+
+
+def kernels_per_run(d: Dims, fp8_weights: bool = False) -> int:
+    """Kernels one whole run enqueues on the current device (plan not counted)."""
+    n = ctypes.c_int32(0)
+    _ok(lib().mla_decode_kernels_per_run(ctypes.byref(d), int(fp8_weights), ctypes.byref(n)),
+        "mla_decode_kernels_per_run")
+    return n.value
 
 
 class MlaDecode:

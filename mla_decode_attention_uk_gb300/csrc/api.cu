@@ -47,6 +47,13 @@ cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, c
                            const PlanHeader* header, const uint8_t* qlo,
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
                            int splits_per_seq, int split_ranges, cudaStream_t st);
+int combine_up_tile();
+cudaError_t launch_combine_up(const CUtensorMap& tm_wuv, int B, int T, int H, const void* ws,
+                              const PlanHeader* header, const int32_t* seq_nsplit,
+                              const int32_t* seq_slot, const uint8_t* qlo,
+                              const __nv_bfloat16* olat, float* lse, float scale,
+                              __nv_bfloat16* out, int32_t* status, int splits_per_seq,
+                              cudaStream_t st);
 }  // namespace mla
 
 namespace {
@@ -246,7 +253,6 @@ const char* mla_decode_status_string(int s) {
   }
 }
 
-int mla_decode_kernels_per_run(void) { return 4; }
 
 int mla_decode_selftest_wait_timeout(int32_t* status, void* stream) {
   if (!status || (reinterpret_cast<uintptr_t>(status) & 3u)) return MLA_DECODE_INVALID_ARG;
@@ -467,6 +473,17 @@ int mla_decode_attend(const mla_decode_dims* d, const void* kv_cache, const int3
       d->num_pages, scale, static_cast<cudaStream_t>(stream)));
 }
 
+// The typical number of splits per sequence, which picks the merge variant of
+// the combine: with fewer work ranges than sequences most rows are unsplit;
+// otherwise a sequence is typically cut into about ranges / batch splits.
+// (Only the speed depends on this guess: every variant computes the same.)
+static int combine_variant(const mla_decode_dims* d, int* ranges, int* splits_per_seq) {
+  const int rc = default_ranges(d, ranges);
+  if (rc) return rc;
+  *splits_per_seq = *ranges < d->batch ? 1 : (*ranges + d->batch - 1) / d->batch;
+  return MLA_DECODE_OK;
+}
+
 // split_only: leave the rows of unsplit sequences alone (their LSE correction
 // is then the up-projection's; see up_project_rows_impl).
 static int combine_impl(const mla_decode_dims* d, float scale, float* lse, void* ws,
@@ -479,19 +496,48 @@ static int combine_impl(const mla_decode_dims* d, float scale, float* lse, void*
   WsLayout L;
   rc = layout_for(d, ws_bytes, &L);
   if (rc) return rc;
-  // With fewer work ranges than sequences most rows are unsplit; otherwise a
-  // sequence is typically cut into about ranges / batch splits.  (Only the
-  // speed depends on this guess: every combine variant computes the same.)
-  int ranges = 0;
-  rc = default_ranges(d, &ranges);
+  int ranges = 0, splits_per_seq = 0;
+  rc = combine_variant(d, &ranges, &splits_per_seq);
   if (rc) return rc;
-  const int splits_per_seq = ranges < d->batch ? 1 : (ranges + d->batch - 1) / d->batch;
   return cuda_rc(launch_combine(at<int32_t>(ws, L.seq_nsplit), at<int32_t>(ws, L.seq_slot), ws,
                                 at<PlanHeader>(ws, L.header), at<uint8_t>(ws, L.qlo),
                                 at<__nv_bfloat16>(ws, L.olat), lse, d->batch, d->q_len,
                                 d->num_heads, scale, splits_per_seq,
                                 split_only ? (ranges > 1 ? ranges - 1 : 1) : 0,
                                 static_cast<cudaStream_t>(stream)));
+}
+
+// Whether a whole run with bf16 weights merges the splits inside the
+// up-projection (combine_up_kernel): fewer than 128 tokens, in 16-token tiles
+// of every head that fit in one wave on the SMs.
+static int run_uses_combine_up(const mla_decode_dims* d, bool* fused) {
+  int sms = 0;
+  const int rc = sm_count(&sms);
+  if (rc) return rc;
+  const int BT = d->batch * d->q_len, nt = combine_up_tile();
+  *fused = BT < 128 && static_cast<int64_t>((BT + nt - 1) / nt) * d->num_heads <= sms;
+  return MLA_DECODE_OK;
+}
+
+// Combine and up-projection of such a run in one launch; out and lse equal
+// those of mla_decode_combine followed by mla_decode_up_project bit for bit.
+static int combine_up_impl(const mla_decode_dims* d, const void* w_uv, float scale, void* out,
+                           float* lse, void* ws, size_t ws_bytes, void* stream) {
+  WsLayout L;
+  int rc = layout_for(d, ws_bytes, &L);
+  if (rc) return rc;
+  int ranges = 0, splits_per_seq = 0;
+  rc = combine_variant(d, &ranges, &splits_per_seq);
+  if (rc) return rc;
+  CUtensorMap tm_w;
+  if (!make_map(&tm_w, w_uv, static_cast<uint64_t>(d->num_heads) * kLora, kVHead, kVHead,
+                kBoxCols, 64, false))
+    return MLA_DECODE_CUDA_ERROR;
+  return cuda_rc(launch_combine_up(
+      tm_w, d->batch, d->q_len, d->num_heads, ws, at<PlanHeader>(ws, L.header),
+      at<int32_t>(ws, L.seq_nsplit), at<int32_t>(ws, L.seq_slot), at<uint8_t>(ws, L.qlo),
+      at<__nv_bfloat16>(ws, L.olat), lse, scale, static_cast<__nv_bfloat16*>(out),
+      at<int32_t>(ws, L.status), splits_per_seq, static_cast<cudaStream_t>(stream)));
 }
 
 int mla_decode_combine(const mla_decode_dims* d, float scale, float* lse, void* ws,
@@ -538,6 +584,12 @@ int mla_decode_run(const mla_decode_dims* d, const void* q, const void* kv_cache
   if (rc) return rc;
   rc = mla_decode_attend(d, kv_cache, block_table, seq_lens, scale, lse, ws, ws_bytes, stream);
   if (rc) return rc;
+  // Small batches: the combine's merges build the up-projection's operand in
+  // shared memory (one launch, no o_lat round trip).
+  bool fused = false;
+  rc = run_uses_combine_up(d, &fused);
+  if (rc) return rc;
+  if (fused) return combine_up_impl(d, w_uv, scale, out, lse, ws, ws_bytes, stream);
   // Large batches: the combine merges split sequences only and the
   // up-projection corrects the lse of the others from the o_lat and q_lo
   // tiles it stages anyway (one read of each instead of two).
@@ -573,6 +625,20 @@ int mla_decode_run_fp8w(const mla_decode_dims* d, const void* q, const void* kv_
     return up_project_rows_impl(d, nullptr, w_uv_fp8, w_uv_scale, scale, out, lse, ws, ws_bytes,
                                 stream);
   return mla_decode_up_project_fp8w(d, w_uv_fp8, w_uv_scale, out, ws, ws_bytes, stream);
+}
+
+int mla_decode_kernels_per_run(const mla_decode_dims* d, int32_t fp8_weights,
+                               int32_t* kernels) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!kernels) return MLA_DECODE_INVALID_ARG;
+  bool fused = false;
+  if (!fp8_weights) {
+    rc = run_uses_combine_up(d, &fused);
+    if (rc) return rc;
+  }
+  *kernels = fused ? 3 : 4;
+  return MLA_DECODE_OK;
 }
 
 int mla_decode_workspace_offsets(const mla_decode_dims* d, int32_t num_ranges,

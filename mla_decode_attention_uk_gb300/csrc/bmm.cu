@@ -40,6 +40,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace mla {
@@ -98,13 +99,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return v;
-}
-
-// Two E4M3 values (the low 16 bits of `bits`, first value in the low byte) of
-// the scaled residual q_lo * 2^10, widened exactly to fp32.
-__device__ __forceinline__ float2 qlo_pair(uint32_t bits) {
-  const __nv_fp8x2_storage_t pr = static_cast<__nv_fp8x2_storage_t>(bits & 0xFFFFu);
-  return __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
 }
 
 // One converter thread's share of a raw FP8 weight tile: k row kr, m (or n)
@@ -1041,6 +1035,175 @@ up_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
 }
 
 
+// Combine and up-projection in one kernel, for small batches whose
+// 16-token tiles of all heads fit in one wave: the up-projection's B operand
+// (the tile's o rows, bf16) is built in shared memory by merge warps, one per
+// token, with the combine's own routines (merge.cuh), so o_lat never goes
+// through global memory and one kernel boundary of the step disappears.
+// Rows of split sequences are merged from their partials, rows of unsplit
+// ones copied from o_lat; either way the row's lse gets its first-order
+// correction, and the result equals, bit for bit, the combine kernel followed
+// by the up-projection.  The W_UV slices (A, all eight 64-deep K stages) load
+// by TMA before the wait for the attention step.
+//   warp 0: TMA producer; warp 1: MMA issuer; warp 2: TMEM owner; warps 0-3:
+//   epilogue (as in bmm_kernel); warps 4-19: merge warps.
+constexpr int kCuNT = 16;                            // tokens per tile
+constexpr int kCuThreads = 128 + 32 * kCuNT;
+constexpr int kCuChunkBytes = kCuNT * 128;           // one 64-deep K chunk of the B tile
+constexpr int kCuSmem = 8 * kABytes + 8 * kCuChunkBytes + 1024;
+
+template <int kUnroll, int kFewN>
+__global__ void __launch_bounds__(kCuThreads, 1)
+combine_up_kernel(const __grid_constant__ CUtensorMap tm_w, int B, int T, int H,
+                  const uint8_t* __restrict__ ws, const PlanHeader* __restrict__ header,
+                  const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict__ seq_slot,
+                  const uint8_t* __restrict__ qlo, const __nv_bfloat16* __restrict__ olat,
+                  float* __restrict__ lse, float scale, __nv_bfloat16* __restrict__ out,
+                  int32_t* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[8], b_ready, done_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  griddep_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BT = B * T, TH = T * H;
+  const int tok0 = blockIdx.x * kCuNT;
+  const int h = blockIdx.y;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const sbase_ptr = smem_raw + (sbase - smem_u32(smem_raw));
+  const uint32_t btile = sbase + 8 * kABytes;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 8; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
+    mbar_init(smem_u32(&b_ready), 1);
+    mbar_init(smem_u32(&done_bar), 1);
+    abort_sh = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_w);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    if (elect_one()) {
+      // W_UV does not depend on the attention step: all of K loads at once.
+      for (int kc = 0; kc < 8; ++kc) {
+        const uint32_t a = sbase + kc * kABytes;
+        const uint32_t fb = smem_u32(&full_bar[kc]);
+        mbar_expect_tx(fb, kABytes);
+        tma_load_2d(a, &tm_w, 0, h * kLora + kc * 64, fb);
+        tma_load_2d(a + kBoxBytes, &tm_w, 64, h * kLora + kc * 64, fb);
+      }
+    }
+  } else if (warp == 1) {
+    if (elect_one()) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kCuNT, /*a_mn=*/true, /*b_mn=*/false);
+      if (mbar_wait(smem_u32(&b_ready), 0, &abort_sh, status)) {
+        for (int kc = 0; kc < 8; ++kc) {
+          if (!mbar_wait(smem_u32(&full_bar[kc]), 0, &abort_sh, status)) break;
+          tc_fence_after();
+          const uint32_t a = sbase + kc * kABytes;
+          const uint32_t b = btile + kc * kCuChunkBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sdesc_sw128(a + kk * 2048, kBoxBytes, 1024);
+            const uint64_t bd = sdesc_sw128(b + kk * 32, 16, 1024);
+            umma_bf16(tmem, ad, bd, idesc, (kc | kk) != 0);
+          }
+        }
+      }
+      umma_commit(smem_u32(&done_bar));
+    }
+  } else if (warp >= 4) {
+    // Merge warp mw: token tok0 + mw, row mw of each K chunk of the B tile
+    // (128-byte rows, 16-byte unit u at u ^ (mw & 7): the layout a TMA box of
+    // the tile would have).
+    const int mw = warp - 4;
+    const int tok = tok0 + mw;
+    if (tok < BT) {
+      const int b = tok / T;
+      const int r = (tok % T) * H + h;
+      const size_t row = static_cast<size_t>(b) * TH + r;
+      const uint32_t rbase = btile + mw * 128;
+      const uint32_t rsw = static_cast<uint32_t>(mw & 7);
+      const int ns = seq_nsplit[b];
+      if (ns <= 1) {
+        // Lane l holds latent columns 16 l .. 16 l + 15: chunk l / 4,
+        // units 2 (l % 4) and 2 (l % 4) + 1.
+        correct_unsplit_row(row, lane, qlo, olat, lse, scale,
+                            [&](const uint4& o0, const uint4& o1) {
+                              const uint32_t cb = rbase + (lane >> 2) * kCuChunkBytes;
+                              const uint32_t u0 = 2u * (lane & 3);
+                              st_shared_v4(cb + ((u0 ^ rsw) << 4), o0.x, o0.y, o0.z, o0.w);
+                              st_shared_v4(cb + (((u0 + 1) ^ rsw) << 4), o1.x, o1.y, o1.z,
+                                           o1.w);
+                            });
+      } else {
+        // Four columns col .. col + 3 (8 bytes): chunk col / 64, unit
+        // (col % 64) / 8, bytes (col % 8) * 2 into it.
+        merge_split_row<kUnroll, kFewN>(
+            b, r, lane, ns, seq_slot[b], B, T, H, ws, header, qlo, lse, scale,
+            [&](int col, const uint2& packed) {
+              const uint32_t u = static_cast<uint32_t>((col & 63) >> 3);
+              st_shared_v2(rbase + (col >> 6) * kCuChunkBytes + ((u ^ rsw) << 4) + (col & 7) * 2,
+                           packed.x, packed.y);
+            });
+      }
+    } else {
+      griddep_wait();
+    }
+    // The B tile goes to the tensor core once all merge warps wrote it.
+    fence_proxy_async_smem();
+    named_bar_sync(1, 32 * kCuNT);
+    if (warp == 4 && lane == 0) mbar_arrive(smem_u32(&b_ready));
+  }
+  __syncwarp();
+
+  // Epilogue (warps 0-3), as in bmm_kernel's up-projection: thread (warp w,
+  // lane i) owns feature 32 w + i, stages a bf16 [token][128] tile in the idle
+  // stage memory, then the four warps copy whole token rows out.
+  if (warp < 4) {
+    const bool have = mbar_wait(smem_u32(&done_bar), 0, &abort_sh, status);
+    tc_fence_after();
+    const int ml = warp * 32 + lane;
+    __nv_bfloat16* const tile = reinterpret_cast<__nv_bfloat16*>(sbase_ptr);
+    const bool go = __all_sync(0xffffffffu, have && !abort_sh);
+    if (go) {
+      uint32_t v[kCuNT];
+      tmem_ld_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16), v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < kCuNT; ++j) tile[j * 128 + ml] = __float2bfloat16_rn(__uint_as_float(v[j]));
+    }
+    named_bar_sync(2, 128);
+    if (go) {
+      const int ntok = min(kCuNT, BT - tok0);
+      for (int i = threadIdx.x; i < ntok * 16; i += 128) {
+        const int tl = i >> 4, ch = i & 15;
+        const size_t row = static_cast<size_t>(tok0 + tl) * H + h;
+        *reinterpret_cast<uint4*>(out + row * kVHead + ch * 8) =
+            *reinterpret_cast<const uint4*>(tile + tl * 128 + ch * 8);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  // After a timeout, let W_UV tiles still in flight land before exiting.
+  if (warp == 0 && lane == 0 && abort_sh)
+    for (int kc = 0; kc < 8; ++kc) mbar_wait_drain(smem_u32(&full_bar[kc]), 0, status);
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 32);
+  }
+}
+
 template <BmmMode MODE, int NT, int kStagesAll = 0>
 cudaError_t launch_bmm_nt(const CUtensorMap& tw, const CUtensorMap& tx, int BT, int H, int K,
                           int Kx, int Mtot, const __nv_bfloat16* q, __nv_bfloat16* hi,
@@ -1093,6 +1256,23 @@ cudaError_t launch_up_rows(const CUtensorMap& tw, const CUtensorMap& to, const C
   e = launch_pdl(up_rows_kernel<W8>, dim3(units < sm_count ? units : sm_count),
                  dim3(C::kThreads), C::kSmem, st, tw, to, tq, tout, BT, T, H, seq_nsplit, lse,
                  scale, status, w8_scale);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int kUnroll, int kFewN>
+cudaError_t launch_cu(const CUtensorMap& tw, int B, int T, int H, const void* ws,
+                      const PlanHeader* header, const int32_t* seq_nsplit,
+                      const int32_t* seq_slot, const uint8_t* qlo, const __nv_bfloat16* olat,
+                      float* lse, float scale, __nv_bfloat16* out, int32_t* status,
+                      cudaStream_t st) {
+  auto kern = combine_up_kernel<kUnroll, kFewN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCuSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((B * T + kCuNT - 1) / kCuNT, H);
+  e = launch_pdl(kern, grid, dim3(kCuThreads), kCuSmem, st, tw, B, T, H,
+                 static_cast<const uint8_t*>(ws), header, seq_nsplit, seq_slot, qlo, olat, lse,
+                 scale, out, status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1170,6 +1350,26 @@ cudaError_t launch_up_project_rows(const CUtensorMap& tm_wuv, const CUtensorMap&
                                           lse, scale, status, wuv_scale, sm_count, st)
                    : launch_up_rows<false>(tm_wuv, tm_olat, tm_qlo, tm_out, BT, T, H, seq_nsplit,
                                            lse, scale, status, nullptr, sm_count, st);
+}
+
+// Small one-wave batches: combine and up-projection in one kernel
+// (bf16 weights).  splits_per_seq picks the same merge variant as the
+// combine step would.
+int combine_up_tile() { return kCuNT; }
+cudaError_t launch_combine_up(const CUtensorMap& tm_wuv, int B, int T, int H, const void* ws,
+                              const PlanHeader* header, const int32_t* seq_nsplit,
+                              const int32_t* seq_slot, const uint8_t* qlo,
+                              const __nv_bfloat16* olat, float* lse, float scale,
+                              __nv_bfloat16* out, int32_t* status, int splits_per_seq,
+                              cudaStream_t st) {
+  if (splits_per_seq <= 1)
+    return launch_cu<1, 2>(tm_wuv, B, T, H, ws, header, seq_nsplit, seq_slot, qlo, olat, lse,
+                           scale, out, status, st);
+  if (splits_per_seq <= 4)
+    return launch_cu<4, 4>(tm_wuv, B, T, H, ws, header, seq_nsplit, seq_slot, qlo, olat, lse,
+                           scale, out, status, st);
+  return launch_cu<4, 0>(tm_wuv, B, T, H, ws, header, seq_nsplit, seq_slot, qlo, olat, lse, scale,
+                         out, status, st);
 }
 
 }  // namespace mla

@@ -48,7 +48,11 @@ def test_status_strings():
         s = L.mla_decode_status_string(code).decode()
         assert s and s != "unknown status"
     assert L.mla_decode_status_string(99).decode() == "unknown status"
-    assert L.mla_decode_kernels_per_run() == 4
+    # Bad dims or a null count fail before any device query (no GPU here).
+    n = ctypes.c_int32(-1)
+    assert L.mla_decode_kernels_per_run(None, 0, ctypes.byref(n)) == 1
+    assert L.mla_decode_kernels_per_run(ctypes.byref(good_dims()), 0, None) == 1
+    assert n.value == -1
 
 
 def good_dims(**kw):

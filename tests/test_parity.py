@@ -173,14 +173,25 @@ def test_one_plan_serves_consecutive_runs_bitwise():
     assert_parity(compare(inp, outs[0].cpu(), lses[0].cpu()), "plan reused")
 
 
-def test_step_calls_equal_run_bitwise():
-    inp = make_inputs(3, [500, 70, 1400], 2, 64, seed=16)
+# Small batches: mla_decode_run merges the splits inside the up-projection
+# (three kernels, see mla_decode_kernels_per_run); the step calls run the
+# combine and the up-projection apart.  Both must agree bit for bit, for each
+# merge variant (mostly unsplit rows: R < B; a few splits; many splits), for
+# ragged last token tiles, and at the largest one-wave size (64 tokens x 16
+# heads, 4 tiles each of 16 heads).
+@pytest.mark.parametrize("B,T,H,R", [(3, 2, 64, 5), (3, 2, 64, 1), (3, 1, 128, 40),
+                                     (10, 2, 32, 4), (64, 1, 16, 0), (8, 1, 128, 0),
+                                     (5, 8, 48, 30)])
+def test_step_calls_equal_run_bitwise(B, T, H, R):
+    g0 = torch.Generator().manual_seed(16 + B + R)
+    lens = torch.randint(1, 3000, (B,), generator=g0).tolist()
+    inp = make_inputs(B, lens, T, H, seed=16)
     dev = torch.device("cuda")
     g = inp.to(dev)
     d = binding.dims_for(g.q, g.cache, g.block_table)
-    m = binding.MlaDecode(d, dev, 5)
-    o1 = torch.empty(3, 2, 64, 128, dtype=torch.bfloat16, device=dev)
-    l1 = torch.empty(3, 2, 64, dtype=torch.float32, device=dev)
+    m = binding.MlaDecode(d, dev, R)
+    o1 = torch.empty(B, T, H, 128, dtype=torch.bfloat16, device=dev)
+    l1 = torch.empty(B, T, H, dtype=torch.float32, device=dev)
     o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
     m.plan(g.seq_lens)
     m.run(g.q, g.cache, g.block_table, g.seq_lens, g.w_uk, g.w_uv, g.scale, o1, l1)
@@ -191,6 +202,24 @@ def test_step_calls_equal_run_bitwise():
     m.up_project(g.w_uv, o2)
     assert m.check() == 0
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert_parity(compare(inp, o1.cpu(), l1.cpu()), "run B=%d T=%d H=%d R=%d" % (B, T, H, R))
+
+
+def test_kernels_per_run():
+    # Fused combine + up-projection for small one-wave batches with bf16
+    # weights only.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+
+    def count(B, T, H, fp8=False):
+        d = binding.Dims(batch=B, q_len=T, num_heads=H, qk_nope=128, qk_rope=64, kv_lora=512,
+                         v_head=128, page_size=64, num_pages=4, max_pages_per_seq=2)
+        return binding.kernels_per_run(d, fp8)
+
+    assert count(64, 1, 16) == 3 and count(8, 1, 128) == 3
+    assert count(8, 1, 128, fp8=True) == 4
+    assert count(128, 1, 128) == 4 and count(64, 2, 16) == 4
+    assert count(112, 1, 32) == (3 if 7 * 32 <= sms else 4)
+    assert count(48, 1, 48) == (3 if 3 * 48 <= sms else 4)
 
 
 @pytest.mark.parametrize("R", [0, 400])
