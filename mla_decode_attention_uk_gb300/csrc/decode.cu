@@ -160,7 +160,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ float alpha_sh[64];
-  __shared__ float inv_l_sh[64];
+  __shared__ __align__(16) float inv_l_sh[64];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x % P.tiles;
@@ -434,6 +434,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int r = tile * kTileRows + srow_c;  // row within the sequence's T*H rows
         const bool row_ok = r < TH;
         const int L = P.seq_len_eff[b];
+        // The epilogue's bookkeeping is loaded now, so that its memory round
+        // trip is not on the path from the piece's last PV to the next
+        // piece's first softmax.
+        const int nsplit = P.seq_nsplit[b];
+        const int split = k - P.seq_first[b];
+        const int slot = P.seq_slot[b];
         const int n_row = row_ok ? L - P.T + r / P.H + 1 : 0;
         float m_used = -INFINITY, l = 0.0f;     // l: this thread's half of the row sum
         const ChunkRange cr(L, pb, pe);
@@ -575,11 +581,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (owner) inv_l_sh[srow_c] = (row_ok && l > 0.0f) ? 1.0f / l : 0.0f;
         if (bar_any(1, 128, bad)) { fail = true; break; }
         tc_fence_after();
-        const int nsplit = P.seq_nsplit[b];
-        const int split = k - P.seq_first[b];
         const size_t row_base = static_cast<size_t>(b) * TH + tile * kTileRows;
         const size_t part_base =
-            nsplit > 1 ? (static_cast<size_t>(P.seq_slot[b] + split) * TH + tile * kTileRows) : 0;
+            nsplit > 1 ? (static_cast<size_t>(slot + split) * TH + tile * kTileRows) : 0;
         const int rows_here = min(kTileRows, TH - tile * kTileRows);
         // Row halves outer, latent blocks inner: each thread keeps the 32
         // reciprocals of its half in registers, so the stores (one row each,
@@ -589,7 +593,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int h2 = 0; h2 < 2 && 32 * h2 < rows_here; ++h2) {  // skip empty row halves
           float il[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) il[j] = inv_l_sh[32 * h2 + j];
+          for (int j = 0; j < 32; j += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(&inv_l_sh[32 * h2 + j]);
+            il[j] = x.x;
+            il[j + 1] = x.y;
+            il[j + 2] = x.z;
+            il[j + 3] = x.w;
+          }
           const int nrow = min(32, rows_here - 32 * h2);
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) {
