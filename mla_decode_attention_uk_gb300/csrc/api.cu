@@ -46,7 +46,8 @@ cudaError_t launch_up_project_rows(const CUtensorMap& tm_wuv, const CUtensorMap&
 cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, const void* ws,
                            const PlanHeader* header, const uint8_t* qlo,
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
-                           int splits_per_seq, int split_ranges, cudaStream_t st);
+                           int splits_per_seq, int split_ranges, int32_t* status,
+                           cudaStream_t st);
 int combine_up_tile();
 cudaError_t launch_combine_up(const CUtensorMap& tm_wuv, int B, int T, int H, const void* ws,
                               const PlanHeader* header, const int32_t* seq_nsplit,
@@ -504,7 +505,7 @@ static int combine_impl(const mla_decode_dims* d, float scale, float* lse, void*
                                 at<__nv_bfloat16>(ws, L.olat), lse, d->batch, d->q_len,
                                 d->num_heads, scale, splits_per_seq,
                                 split_only ? (ranges > 1 ? ranges - 1 : 1) : 0,
-                                static_cast<cudaStream_t>(stream)));
+                                at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream)));
 }
 
 // Whether a whole run with bf16 weights merges the splits inside the

@@ -27,6 +27,18 @@ namespace {
 
 constexpr int kCombThreads = 256;
 
+// Bulk copy (no tensor map) of `bytes` from global to shared memory,
+// completing on an mbarrier; both addresses and the size are multiples of 16
+// bytes.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 constexpr int kRowsPerCta = kCombThreads / 32;
 
 // At least three CTAs per SM: the unrolled instantiations then get up to 85
@@ -66,37 +78,97 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
 // unsplit rows itself.  Sequence b is split exactly when a work range starts
 // inside it, and the first such range is k = seq_first[b] + 1, so walking the
 // ranges visits every split sequence once; the grid's y dimension strides
-// over them.  (A kernel of its own: the loop around the merge would cost the
-// other instantiations registers; its grid is small, so it may use as many
-// as it needs.)
+// over them and its x dimension over blocks of kSplitRows rows.  A CTA that
+// finds a split sequence brings the partial rows of its row block into
+// shared memory with one bulk copy per split (the rows of one split are
+// contiguous: 16 x 2 KB), so all of a block's partials are in flight at once
+// instead of the few that one warp per row keeps in registers (measured:
+// that form cost 11.7 us of a 512-token x 128-head step, latency-bound at
+// one or two CTAs per SM).  Sequences with more splits than are staged read
+// their partials from global memory; the merge arithmetic is the same either
+// way.  (A kernel of its own: the loop around the merge would cost the other
+// instantiations registers; its grid is small, so it may use what it
+// needs: two CTAs per SM, one for the variant that keeps four splits'
+// partials in registers.)
+constexpr int kSplitRows = 16;
+
 template <int kUnroll, int kFewN>
-__global__ void __launch_bounds__(kCombThreads, 1)
+__global__ void __launch_bounds__(kCombThreads, kFewN == 4 ? 1 : 2)
 combine_split_kernel(const int32_t* __restrict__ seq_nsplit,
                      const int32_t* __restrict__ seq_slot, const uint8_t* __restrict__ ws,
                      const PlanHeader* __restrict__ header, int B, int T, int H,
                      const uint8_t* __restrict__ qlo, __nv_bfloat16* __restrict__ olat,
-                     float* __restrict__ lse_out, float scale) {
+                     float* __restrict__ lse_out, float scale, int stage_splits,
+                     int32_t* __restrict__ status) {
+  extern __shared__ __align__(128) uint8_t stage_raw[];
+  __shared__ __align__(8) uint64_t full_bar;
+  __shared__ int abort_sh;
   // The plan is complete when this kernel starts (as in combine_kernel).
   griddep_launch_dependents();
   const int TH = T * H;
-  const int r = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r < TH) {
-    const WsLayout L = make_layout(B, T, H, header->num_ranges);
-    const int32_t* __restrict__ range_b = reinterpret_cast<const int32_t*>(ws + L.range_b);
-    const int32_t* __restrict__ range_p = reinterpret_cast<const int32_t*>(ws + L.range_p);
-    const int32_t* __restrict__ seq_first = reinterpret_cast<const int32_t*>(ws + L.seq_first);
-    for (int k = blockIdx.y + 1; k < L.num_ranges; k += gridDim.y) {
-      const int b = range_b[k];
-      if (b >= B || range_p[k] == 0 || seq_first[b] + 1 != k) continue;
-      const size_t row_o = static_cast<size_t>(b) * TH + r;
-      merge_split_row<kUnroll, kFewN>(
-          b, r, lane, seq_nsplit[b], seq_slot[b], B, T, H, ws, header, qlo, lse_out, scale,
-          [&](int col, const uint2& packed) {
-            *reinterpret_cast<uint2*>(olat + row_o * kLora + col) = packed;
-          });
-    }
+  const int r0 = blockIdx.x * kSplitRows;
+  const int nrows = min(kSplitRows, TH - r0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&full_bar), 1);
+    abort_sh = 0;
+    fence_mbar_init();
   }
+  __syncthreads();
+  const float4* const stage = reinterpret_cast<const float4*>(stage_raw);
+  const WsLayout L = make_layout(B, T, H, header->num_ranges);
+  const int32_t* __restrict__ range_b = reinterpret_cast<const int32_t*>(ws + L.range_b);
+  const int32_t* __restrict__ range_p = reinterpret_cast<const int32_t*>(ws + L.range_p);
+  const int32_t* __restrict__ seq_first = reinterpret_cast<const int32_t*>(ws + L.seq_first);
+  uint32_t phase = 0;
+  int issued = 0;  // bulk-copy rounds started by thread 0
+  for (int k = blockIdx.y + 1; k < L.num_ranges && nrows > 0; k += gridDim.y) {
+    if (abort_sh) break;  // a staging wait timed out (read after a barrier: uniform)
+    const int b = range_b[k];
+    if (b >= B || range_p[k] == 0 || seq_first[b] + 1 != k) continue;  // the same for the CTA
+    const int ns = seq_nsplit[b], slot0 = seq_slot[b];
+    const bool staged = ns <= stage_splits;
+    bool ok = true;
+    if (staged) {
+      if (threadIdx.x == 0) {
+        griddep_wait();  // the partials come from the attention step
+        fence_proxy_async_smem();  // earlier reads of the staging area come first
+        const float* opart = reinterpret_cast<const float*>(ws + L.opart);
+        const uint32_t bytes = static_cast<uint32_t>(nrows) * kLora * 4;
+        mbar_expect_tx(smem_u32(&full_bar), bytes * ns);
+        for (int s = 0; s < ns; ++s)
+          bulk_load_g2s(smem_u32(stage_raw) + s * kSplitRows * kLora * 4,
+                        opart + (static_cast<size_t>(slot0 + s) * TH + r0) * kLora, bytes,
+                        smem_u32(&full_bar));
+        ++issued;
+      }
+      ok = mbar_wait(smem_u32(&full_bar), phase, &abort_sh, status);
+      phase ^= 1;
+    }
+    if (ok) {
+      for (int rr = warp; rr < nrows; rr += kCombThreads / 32) {
+        const int r = r0 + rr;
+        const size_t row_o = static_cast<size_t>(b) * TH + r;
+        auto sink = [&](int col, const uint2& packed) {
+          *reinterpret_cast<uint2*>(olat + row_o * kLora + col) = packed;
+        };
+        if (staged) {
+          merge_split_row<kUnroll, kFewN>(
+              b, r, lane, ns, slot0, B, T, H, ws, header, qlo, lse_out, scale, sink,
+              [&](const float*, int, int s, int, int) {
+                return stage + (s * kSplitRows + rr) * (kLora / 4);
+              });
+        } else {
+          merge_split_row<kUnroll, kFewN>(b, r, lane, ns, slot0, B, T, H, ws, header, qlo,
+                                          lse_out, scale, sink);
+        }
+      }
+    }
+    __syncthreads();  // the staging area is reused for the next sequence
+  }
+  // After a timeout, let a bulk copy still in flight land before exiting.
+  if (threadIdx.x == 0 && abort_sh && issued > 0)
+    mbar_wait_drain(smem_u32(&full_bar), (issued - 1) & 1, status);
   griddep_wait();
 }
 
@@ -105,23 +177,36 @@ combine_split_kernel(const int32_t* __restrict__ seq_nsplit,
 cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, const void* ws,
                            const PlanHeader* header, const uint8_t* qlo,
                            __nv_bfloat16* olat, float* lse, int B, int T, int H, float scale,
-                           int splits_per_seq, int split_ranges, cudaStream_t st) {
-  // split_ranges > 0: split sequences only, the grid's y dimension striding
-  // over that many work ranges (the planner's count or any other).
-  const bool split_only = split_ranges > 0;
-  dim3 grid((T * H + kRowsPerCta - 1) / kRowsPerCta, split_only ? split_ranges : B);
+                           int splits_per_seq, int split_ranges, int32_t* status,
+                           cudaStream_t st) {
   // splits_per_seq: work ranges per sequence, rounded up (the host's guess of
   // the typical split count; only the speed depends on it).  A split-only
-  // launch takes the same variant as the full combine would, so a split
-  // row's o_lat is the same bit for bit either way.
-  auto kern = splits_per_seq <= 1
-                  ? (split_only ? combine_split_kernel<1, 2> : combine_kernel<1, 2>)
-              : splits_per_seq <= 4
-                  ? (split_only ? combine_split_kernel<4, 4> : combine_kernel<4, 4>)
-                  : (split_only ? combine_split_kernel<4, 0> : combine_kernel<4, 0>);
-  cudaError_t e = launch_pdl(kern, grid, dim3(kCombThreads), 0, st, seq_nsplit, seq_slot,
-                             static_cast<const uint8_t*>(ws), header, B, T, H, qlo, olat, lse,
-                             scale);
+  // launch takes the same merge variant as the full combine would, so a
+  // split row's o_lat is the same bit for bit either way.
+  cudaError_t e;
+  if (split_ranges > 0) {
+    // Split sequences only, the grid's y dimension striding over that many
+    // work ranges (the planner's count or any other); partials of up to
+    // stage_splits splits are staged in shared memory.
+    const int stage_splits = splits_per_seq <= 1 ? 2 : (splits_per_seq <= 4 ? 4 : 6);
+    const int smem = stage_splits * kSplitRows * kLora * 4;
+    auto kern = splits_per_seq <= 1   ? combine_split_kernel<1, 2>
+                : splits_per_seq <= 4 ? combine_split_kernel<4, 4>
+                                      : combine_split_kernel<4, 0>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((T * H + kSplitRows - 1) / kSplitRows, split_ranges);
+    e = launch_pdl(kern, grid, dim3(kCombThreads), smem, st, seq_nsplit, seq_slot,
+                   static_cast<const uint8_t*>(ws), header, B, T, H, qlo, olat, lse, scale,
+                   stage_splits, status);
+  } else {
+    auto kern = splits_per_seq <= 1   ? combine_kernel<1, 2>
+                : splits_per_seq <= 4 ? combine_kernel<4, 4>
+                                      : combine_kernel<4, 0>;
+    dim3 grid((T * H + kRowsPerCta - 1) / kRowsPerCta, B);
+    e = launch_pdl(kern, grid, dim3(kCombThreads), 0, st, seq_nsplit, seq_slot,
+                   static_cast<const uint8_t*>(ws), header, B, T, H, qlo, olat, lse, scale);
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

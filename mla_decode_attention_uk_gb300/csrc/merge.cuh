@@ -30,19 +30,30 @@ __device__ __forceinline__ float2 qlo_pair(uint32_t bits) {
   const __nv_fp8x2_storage_t pr = static_cast<__nv_fp8x2_storage_t>(bits & 0xFFFFu);
   return __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
 }
+// The partial output row of split s, read where the attention step wrote it
+// (the default source of merge_split_row).
+struct GlobalPartRows {
+  __device__ const float4* operator()(const float* opart, int slot0, int s, int TH, int r) const {
+    return reinterpret_cast<const float4*>(opart +
+                                           (static_cast<size_t>(slot0 + s) * TH + r) * kLora);
+  }
+};
+
 // One warp merges row r of split sequence b (ns splits, partial slots from
 // slot0): lse and o over the splits, o as bf16 (sink(col, four bf16 of
 // columns col .. col + 3), for col = (32 q + lane) * 4), and the lse with its
 // first-order correction.  Rows of at most kFewN splits load every split's
 // lse and partial output at once; others go through a split loop unrolled
-// kUnroll times.
-template <int kUnroll, int kFewN, class Sink>
+// kUnroll times.  part_rows(opart, slot0, s, TH, r) gives split s's partial
+// row (512 fp32 as 128 float4): global memory, or a copy staged in shared
+// memory; the arithmetic is the same either way.
+template <int kUnroll, int kFewN, class Sink, class PartRows = GlobalPartRows>
 __device__ __forceinline__ void merge_split_row(int b, int r, int lane, int ns, int slot0, int B,
                                                 int T, int H, const uint8_t* __restrict__ ws,
                                                 const PlanHeader* __restrict__ header,
                                                 const uint8_t* __restrict__ qlo,
                                                 float* __restrict__ lse_out, float scale,
-                                                Sink&& sink) {
+                                                Sink&& sink, PartRows part_rows = PartRows()) {
   const int TH = T * H;
   const size_t row = static_cast<size_t>(b) * TH + r;
   uint32_t lo_raw[4];  // 4 E4M3 residuals per (q, lane): columns (32 q + lane) * 4 ..
@@ -70,7 +81,7 @@ __device__ __forceinline__ void merge_split_row(int b, int r, int lane, int ns, 
       if (s < ns) {
         const size_t srow = static_cast<size_t>(slot0 + s) * TH + r;
         l[s] = lpart[srow];
-        const float4* src = reinterpret_cast<const float4*>(opart + srow * kLora);
+        const float4* src = part_rows(opart, slot0, s, TH, r);
 #pragma unroll
         for (int q = 0; q < 4; ++q) v[s][q] = src[q * 32 + lane];
       }
@@ -123,8 +134,7 @@ __device__ __forceinline__ void merge_split_row(int b, int r, int lane, int ns, 
 #pragma unroll kUnroll
       for (int i = 0; i < n; ++i) {
         const float w = __shfl_sync(0xffffffffu, wl, i);
-        const float4* src = reinterpret_cast<const float4*>(
-            opart + (static_cast<size_t>(slot0 + s0 + i) * TH + r) * kLora);
+        const float4* src = part_rows(opart, slot0, s0 + i, TH, r);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float4 v = src[q * 32 + lane];
