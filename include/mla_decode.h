@@ -156,8 +156,8 @@ int mla_decode_run(const mla_decode_dims* dims, const void* q, const void* kv_ca
  *   absorb:     q, w_uk            -> q_lat (bf16 part, and the residual q_lo
  *                                     as E4M3 of q_lo * 2^10, workspace)
  *   attend:     q_lat, cache, ...  -> o_lat + lse (from the bf16 part of q_lat)
- *                                     for unsplit sequences, fp32 partials for
- *                                     split ones
+ *                                     for unsplit sequences, partials (o as
+ *                                     bf16, lse as fp32) for split ones
  *   combine:    partials           -> o_lat + lse for split sequences; then
  *                                     every row's lse += scale * (q_lo . o_lat),
  *                                     the first-order correction for the bf16

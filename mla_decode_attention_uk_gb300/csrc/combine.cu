@@ -81,7 +81,7 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
 // over them and its x dimension over blocks of kSplitRows rows.  A CTA that
 // finds a split sequence brings the partial rows of its row block into
 // shared memory with one bulk copy per split (the rows of one split are
-// contiguous: 16 x 2 KB), so all of a block's partials are in flight at once
+// contiguous: 16 x 1 KB), so all of a block's partials are in flight at once
 // instead of the few that one warp per row keeps in registers (measured:
 // that form cost 11.7 us of a 512-token x 128-head step, latency-bound at
 // one or two CTAs per SM).  Sequences with more splits than are staged read
@@ -115,7 +115,7 @@ combine_split_kernel(const int32_t* __restrict__ seq_nsplit,
     fence_mbar_init();
   }
   __syncthreads();
-  const float4* const stage = reinterpret_cast<const float4*>(stage_raw);
+  const uint2* const stage = reinterpret_cast<const uint2*>(stage_raw);
   const WsLayout L = make_layout(B, T, H, header->num_ranges);
   const int32_t* __restrict__ range_b = reinterpret_cast<const int32_t*>(ws + L.range_b);
   const int32_t* __restrict__ range_p = reinterpret_cast<const int32_t*>(ws + L.range_p);
@@ -133,11 +133,11 @@ combine_split_kernel(const int32_t* __restrict__ seq_nsplit,
       if (threadIdx.x == 0) {
         griddep_wait();  // the partials come from the attention step
         fence_proxy_async_smem();  // earlier reads of the staging area come first
-        const float* opart = reinterpret_cast<const float*>(ws + L.opart);
-        const uint32_t bytes = static_cast<uint32_t>(nrows) * kLora * 4;
+        const __nv_bfloat16* opart = reinterpret_cast<const __nv_bfloat16*>(ws + L.opart);
+        const uint32_t bytes = static_cast<uint32_t>(nrows) * kLora * 2;
         mbar_expect_tx(smem_u32(&full_bar), bytes * ns);
         for (int s = 0; s < ns; ++s)
-          bulk_load_g2s(smem_u32(stage_raw) + s * kSplitRows * kLora * 4,
+          bulk_load_g2s(smem_u32(stage_raw) + s * kSplitRows * kLora * 2,
                         opart + (static_cast<size_t>(slot0 + s) * TH + r0) * kLora, bytes,
                         smem_u32(&full_bar));
         ++issued;
@@ -155,7 +155,7 @@ combine_split_kernel(const int32_t* __restrict__ seq_nsplit,
         if (staged) {
           merge_split_row<kUnroll, kFewN>(
               b, r, lane, ns, slot0, B, T, H, ws, header, qlo, lse_out, scale, sink,
-              [&](const float*, int, int s, int, int) {
+              [&](const __nv_bfloat16*, int, int s, int, int) {
                 return stage + (s * kSplitRows + rr) * (kLora / 4);
               });
         } else {
@@ -188,8 +188,8 @@ cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, c
     // Split sequences only, the grid's y dimension striding over that many
     // work ranges (the planner's count or any other); partials of up to
     // stage_splits splits are staged in shared memory.
-    const int stage_splits = splits_per_seq <= 1 ? 2 : (splits_per_seq <= 4 ? 4 : 6);
-    const int smem = stage_splits * kSplitRows * kLora * 4;
+    const int stage_splits = splits_per_seq <= 1 ? 4 : (splits_per_seq <= 4 ? 8 : 12);
+    const int smem = stage_splits * kSplitRows * kLora * 2;
     auto kern = splits_per_seq <= 1   ? combine_split_kernel<1, 2>
                 : splits_per_seq <= 4 ? combine_split_kernel<4, 4>
                                       : combine_split_kernel<4, 0>;

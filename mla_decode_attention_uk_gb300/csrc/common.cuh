@@ -95,7 +95,7 @@ struct WsLayout {
   size_t range_b;     // int32 [R+1]                     (R-dependent from here on)
   size_t range_p;     // int32 [R+1]
   size_t lpart;       // fp32 [slots, T*H]       split partial LSE (natural log)
-  size_t opart;       // fp32 [slots, T*H, 512]  split partial outputs (normalised)
+  size_t opart;       // bf16 [slots, T*H, 512]  split partial outputs (normalised)
   size_t total;
   int32_t num_ranges;
   int32_t max_slots;
@@ -122,7 +122,7 @@ __host__ __device__ inline WsLayout make_layout(int B, int T, int H, int R) {
   L.range_b = take(sizeof(int32_t) * (R + 1));
   L.range_p = take(sizeof(int32_t) * (R + 1));
   L.lpart = take(static_cast<size_t>(slots) * T * H * 4);
-  L.opart = take(static_cast<size_t>(slots) * T * H * kLora * 4);
+  L.opart = take(static_cast<size_t>(slots) * T * H * kLora * 2);
   L.total = o;
   L.num_ranges = R;
   L.max_slots = slots;

@@ -33,7 +33,7 @@
 //     page is written into that page's RoPE box (dead once QK^T is done), so
 //     every page in flight has its own P^T buffer at no extra shared memory.
 //   * Epilogue (warps 4-7): O / l to bf16 o_lat plus lse for unsplit sequences,
-//     or fp32 partials for split ones.
+//     or bf16 partial outputs (fp32 lse) for split ones.
 // Warp roles: 0 TMA producer, 1-2 QK^T issuers (K halves; warp 2 also owns
 // TMEM), 3 and 8 PV issuers (latent halves), 4-7 softmax and epilogue.  The
 // issuers work from precomputed descriptors, so one MMA costs an add and the
@@ -84,7 +84,7 @@ struct DecodeParams {
   const int32_t* seq_slot;
   __nv_bfloat16* olat;       // [B*T*H, 512]
   float* lse;                // [B*T*H]
-  float* opart;              // [slots, T*H, 512]
+  __nv_bfloat16* opart;      // [slots, T*H, 512]
   float* lpart;              // [slots, T*H]
   int32_t* status;
   int B, T, H, max_pages, num_pages, tiles, q_box_rows, num_slots;
@@ -208,7 +208,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     P.range_b = reinterpret_cast<const int32_t*>(P.ws + L.range_b);
     P.range_p = reinterpret_cast<const int32_t*>(P.ws + L.range_p);
     P.lpart = reinterpret_cast<float*>(P.ws + L.lpart);
-    P.opart = reinterpret_cast<float*>(P.ws + L.opart);
+    P.opart = reinterpret_cast<__nv_bfloat16*>(P.ws + L.opart);
   }
   if (warp == 2) {
     tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
@@ -607,17 +607,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             uint32_t v[32];
             tmem_ld_x32(tmem + lane_off + kTmemO + 64 * m + 32 * h2, v);
             tmem_wait_ld();
-            if (nsplit > 1) {
-              float* dst = P.opart + (part_base + 32 * h2) * kLora + lat;
+            // bf16 either way: o_lat of an unsplit sequence, or the partial
+            // output of a split one (the merge rounds to bf16 again; bf16
+            // partials halve the bytes of the split rows' round trip).
+            __nv_bfloat16* dst = (nsplit > 1 ? P.opart : P.olat) +
+                                 ((nsplit > 1 ? part_base : row_base) + 32 * h2) * kLora + lat;
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j < nrow) dst[j * kLora] = __uint_as_float(v[j]) * il[j];
-            } else {
-              __nv_bfloat16* dst = P.olat + (row_base + 32 * h2) * kLora + lat;
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j < nrow) dst[j * kLora] = __float2bfloat16_rn(__uint_as_float(v[j]) * il[j]);
-            }
+            for (int j = 0; j < 32; ++j)
+              if (j < nrow) dst[j * kLora] = __float2bfloat16_rn(__uint_as_float(v[j]) * il[j]);
           }
         }
         tc_fence_before();

@@ -30,14 +30,21 @@ __device__ __forceinline__ float2 qlo_pair(uint32_t bits) {
   const __nv_fp8x2_storage_t pr = static_cast<__nv_fp8x2_storage_t>(bits & 0xFFFFu);
   return __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3)));
 }
-// The partial output row of split s, read where the attention step wrote it
-// (the default source of merge_split_row).
+// The partial output row of split s (512 bf16), read where the attention
+// step wrote it (the default source of merge_split_row).  uint2 = four bf16.
 struct GlobalPartRows {
-  __device__ const float4* operator()(const float* opart, int slot0, int s, int TH, int r) const {
-    return reinterpret_cast<const float4*>(opart +
-                                           (static_cast<size_t>(slot0 + s) * TH + r) * kLora);
+  __device__ const uint2* operator()(const __nv_bfloat16* opart, int slot0, int s, int TH,
+                                     int r) const {
+    return reinterpret_cast<const uint2*>(opart +
+                                          (static_cast<size_t>(slot0 + s) * TH + r) * kLora);
   }
 };
+// Four bf16 (low half first) widened exactly to fp32.
+__device__ __forceinline__ float4 bf16x4_to_float4(uint2 u) {
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
 
 // One warp merges row r of split sequence b (ns splits, partial slots from
 // slot0): lse and o over the splits, o as bf16 (sink(col, four bf16 of
@@ -45,7 +52,7 @@ struct GlobalPartRows {
 // first-order correction.  Rows of at most kFewN splits load every split's
 // lse and partial output at once; others go through a split loop unrolled
 // kUnroll times.  part_rows(opart, slot0, s, TH, r) gives split s's partial
-// row (512 fp32 as 128 float4): global memory, or a copy staged in shared
+// row (512 bf16 as 128 uint2): global memory, or a copy staged in shared
 // memory; the arithmetic is the same either way.
 template <int kUnroll, int kFewN, class Sink, class PartRows = GlobalPartRows>
 __device__ __forceinline__ void merge_split_row(int b, int r, int lane, int ns, int slot0, int B,
@@ -62,7 +69,7 @@ __device__ __forceinline__ void merge_split_row(int b, int r, int lane, int ns, 
     lo_raw[q] = *reinterpret_cast<const uint32_t*>(qlo + row * kLora + (q * 32 + lane) * 4);
   griddep_wait();
   const WsLayout L = make_layout(B, T, H, header->num_ranges);
-  const float* __restrict__ opart = reinterpret_cast<const float*>(ws + L.opart);
+  const __nv_bfloat16* __restrict__ opart = reinterpret_cast<const __nv_bfloat16*>(ws + L.opart);
   const float* __restrict__ lpart = reinterpret_cast<const float*>(ws + L.lpart);
 
   float4 acc[4];
@@ -81,9 +88,9 @@ __device__ __forceinline__ void merge_split_row(int b, int r, int lane, int ns, 
       if (s < ns) {
         const size_t srow = static_cast<size_t>(slot0 + s) * TH + r;
         l[s] = lpart[srow];
-        const float4* src = part_rows(opart, slot0, s, TH, r);
+        const uint2* src = part_rows(opart, slot0, s, TH, r);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[s][q] = src[q * 32 + lane];
+        for (int q = 0; q < 4; ++q) v[s][q] = bf16x4_to_float4(src[q * 32 + lane]);
       }
     }
     float m = l[0];
@@ -134,10 +141,10 @@ __device__ __forceinline__ void merge_split_row(int b, int r, int lane, int ns, 
 #pragma unroll kUnroll
       for (int i = 0; i < n; ++i) {
         const float w = __shfl_sync(0xffffffffu, wl, i);
-        const float4* src = part_rows(opart, slot0, s0 + i, TH, r);
+        const uint2* src = part_rows(opart, slot0, s0 + i, TH, r);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float4 v = src[q * 32 + lane];
+          const float4 v = bf16x4_to_float4(src[q * 32 + lane]);
           acc[q].x += w * v.x;
           acc[q].y += w * v.y;
           acc[q].z += w * v.z;

@@ -32,8 +32,8 @@ int main(void) {
   size_t bytes = 0;
   CHECK(mla_decode_workspace_size_ex(&d, 152, &bytes) == MLA_DECODE_OK);
   /* q_lat (bf16), q_lo (E4M3 bytes) and o_lat (bf16) for 1024 rows, plus 304
-     partial slots of 16 rows. */
-  CHECK(bytes >= (size_t)1024 * (576 * 2 + 512 + 512 * 2) + (size_t)304 * 16 * 513 * 4);
+     partial slots of 16 rows (bf16 o, fp32 lse). */
+  CHECK(bytes >= (size_t)1024 * (576 * 2 + 512 + 512 * 2) + (size_t)304 * 16 * (512 * 2 + 4));
 
   mla_decode_dims bad = d;
   bad.kv_lora = 256;

@@ -159,8 +159,8 @@ def test_workspace_layout_holds_the_documented_buffers(B, T, H, R):
     # With an explicit range count the sizing needs no device.  The header
     # documents q_lat bf16 [B*T*H, 576], q_lo E4M3 bytes [B*T*H, 512] and
     # o_lat bf16 [B*T*H, 512];
-    # the split partials (two slots per range: fp32 lse [T*H] and o [T*H, 512]
-    # each) come after them.
+    # the split partials (two slots per range: fp32 lse [T*H] and bf16 o
+    # [T*H, 512] each) come after them.
     L = binding.lib()
     d = good_dims(batch=B, q_len=T, num_heads=H)
     n = ctypes.c_size_t(0)
@@ -173,15 +173,15 @@ def test_workspace_layout_holds_the_documented_buffers(B, T, H, R):
     assert header + 16 <= q_lat  # plan header (four int32) before the buffers
     assert q_lat + rows * 576 * 2 <= q_lo
     assert q_lo + rows * 512 <= o_lat
-    partials = 2 * R * T * H * (512 + 1) * 4
+    partials = 2 * R * T * H * (512 * 2 + 4)
     assert o_lat + rows * 512 * 2 + partials <= n.value
     # Each extra range adds two partial slots (and its range bounds): at least
-    # the two fp32 [T*H, 512] outputs; the small arrays may fit in the 256-byte
+    # the two bf16 [T*H, 512] outputs; the small arrays may fit in the 256-byte
     # rounding of their regions.
     n2 = ctypes.c_size_t(0)
     assert L.mla_decode_workspace_size_ex(ctypes.byref(d), R + 1, ctypes.byref(n2)) == 0
     grow = n2.value - n.value
-    assert 2 * T * H * 512 * 4 <= grow <= 2 * T * H * (512 + 1) * 4 + 4 * 256
+    assert 2 * T * H * 512 * 2 <= grow <= 2 * T * H * (512 * 2 + 4) + 4 * 256
     # Without a device the default range count cannot be known.
     assert L.mla_decode_workspace_size_ex(ctypes.byref(d), -1, ctypes.byref(n2)) == 1
     assert L.mla_decode_workspace_size_ex(ctypes.byref(d), 65537, ctypes.byref(n2)) == 1
