@@ -86,7 +86,10 @@ typedef enum {
 } mla_decode_status;
 
 /* Bytes of device workspace needed for `dims` on the current device, with the
- * default number of work ranges (one per resident decode CTA group).
+ * default number of work ranges (one per resident decode CTA group; when the
+ * groups that hold all 64-row tiles of a sequence would leave 3 % or more of
+ * the SMs idle, groups hold fewer tiles and the count is the smallest that
+ * gives every group the same number of (range, tile set) tasks).
  * The workspace holds the split-KV plan, the absorbed query (step 1 above),
  * the latent output and the partial results of key ranges that the log-sum-exp
  * merge combines ("DeepSeek publica FlashMLA como codigo abierto": FlashMLA's

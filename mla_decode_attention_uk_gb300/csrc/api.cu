@@ -30,8 +30,8 @@ cudaError_t launch_up_project(const CUtensorMap& tm_wuv, const CUtensorMap& tm_o
                               const uint8_t* wuv8, const float* wuv_scale, bool one_wave);
 int decode_tiles(int T, int H);
 int decode_q_box_rows(int T, int H);
-cudaError_t decode_max_groups(int T, int H, int sm_count, int* groups);
-cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int groups,
+cudaError_t decode_default_ranges(int T, int H, int sm_count, int* ranges);
+cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int sm_count,
                           const int32_t* block_table, const int32_t* seq_len_eff,
                           const PlanHeader* header, void* ws, const int32_t* seq_first,
                           const int32_t* seq_nsplit, const int32_t* seq_slot,
@@ -174,8 +174,10 @@ int check_dims(const mla_decode_dims* d) {
   return MLA_DECODE_OK;
 }
 
-// Default number of work ranges = co-resident decode CTA groups (one group =
-// the CTAs covering all query rows of a sequence).  Cached per device and
+// Default number of work ranges: one per co-resident decode CTA group (a
+// group = the CTAs covering all query rows of a sequence), or, when those
+// groups would leave SMs idle, enough for every SM to take the same number of
+// (range, tile set) tasks (decode_default_ranges).  Cached per device and
 // (q_len, heads).
 int g_groups[kMaxDevices][kMaxQLen + 1][9];
 std::mutex g_groups_mu;
@@ -190,10 +192,10 @@ int default_ranges(const mla_decode_dims* d, int* R) {
   std::lock_guard<std::mutex> lock(g_groups_mu);
   int& slot = g_groups[dev][d->q_len][hi];
   if (slot <= 0) {
-    int groups = 0;
-    if (decode_max_groups(d->q_len, d->num_heads, sms, &groups) != cudaSuccess)
+    int ranges = 0;
+    if (decode_default_ranges(d->q_len, d->num_heads, sms, &ranges) != cudaSuccess)
       return cuda_rc(cudaErrorUnknown);
-    slot = groups;
+    slot = ranges;
   }
   *R = slot;
   return MLA_DECODE_OK;
@@ -463,11 +465,11 @@ int mla_decode_attend(const mla_decode_dims* d, const void* kv_cache, const int3
       !make_map(&tm_c, kv_cache, static_cast<uint64_t>(d->num_pages) * kPage, kDqk, kDqk,
                 kBoxCols, kPage, true))
     return MLA_DECODE_CUDA_ERROR;
-  int groups = 0;
-  rc = default_ranges(d, &groups);
+  int sms = 0;
+  rc = sm_count(&sms);
   if (rc) return rc;
   return cuda_rc(launch_decode(
-      tm_q, tm_c, groups, block_table, at<int32_t>(ws, L.seq_len_eff), at<PlanHeader>(ws, L.header),
+      tm_q, tm_c, sms, block_table, at<int32_t>(ws, L.seq_len_eff), at<PlanHeader>(ws, L.header),
       ws, at<int32_t>(ws, L.seq_first), at<int32_t>(ws, L.seq_nsplit), at<int32_t>(ws, L.seq_slot),
       at<__nv_bfloat16>(ws, L.olat), lse,
       at<int32_t>(ws, L.status), d->batch, d->q_len, d->num_heads, d->max_pages_per_seq,

@@ -9,14 +9,15 @@
 // range by key range, in the FlashAttention manner that page credits, and key
 // ranges cut by the planner are merged later by their log-sum-exp.
 //
-// GB300 mapping (one CTA = 64 query rows of one sequence, one work range):
+// GB300 mapping (one CTA = 64 query rows of one sequence at a time, over the
+// work ranges it is dealt; see decode_shape for how CTAs are grouped):
 //   * Keys stream page by page: the TMA producer gathers a 64-token page as 9
 //     boxes of 64 x 64 bf16 (128B swizzle) into a ring of 72 KB slots (two fit
 //     next to the query tile), looking the physical page up in the block
 //     table.  Slots fill and empty box by box: QK^T starts on a page's first
 //     boxes while the rest land, and the next page's boxes load as soon as
 //     their release group of the slot is free.  When the query rows of a
-//     sequence span 2 or 4 CTAs (tiles), those CTAs stream the same pages at
+//     sequence span several CTAs (tiles), those CTAs stream the same pages at
 //     about the same time and the second read of a page is served by L2; they
 //     are not coupled (a cluster sharing pages by multicast made every slot
 //     refill wait for the slower CTA, which cost more than it saved).
@@ -87,7 +88,8 @@ struct DecodeParams {
   __nv_bfloat16* opart;      // [slots, T*H, 512]
   float* lpart;              // [slots, T*H]
   int32_t* status;
-  int B, T, H, max_pages, num_pages, tiles, q_box_rows, num_slots;
+  int B, T, H, max_pages, num_pages, q_box_rows, num_slots;
+  int tpg, sets;             // tiles per CTA group; tile sets per sequence
   float scale, scale_log2;
 };
 
@@ -142,6 +144,11 @@ struct ChunkRange {
   __device__ int key0(int i) const { return (pbeg + i) * kPage; }
 };
 
+// kSets: a CTA group holds only some of a sequence's tiles (P.sets > 1).
+// Without it the task loops below reduce at compile time to one range after
+// another for a fixed tile (measured: the general loops cost 0.3 % of the
+// attention time on shapes that do not need them).
+template <bool kSets>
 __global__ void __launch_bounds__(kDecThreads, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
               DecodeParams P) {
@@ -163,9 +170,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   __shared__ __align__(16) float inv_l_sh[64];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x % P.tiles;
-  const int k0 = blockIdx.x / P.tiles;
-  const int G = gridDim.x / P.tiles;
+  // Work: tasks v = (range k, tile set), v = k * sets + set, dealt round
+  // robin to the CTA groups; a group's CTA ti takes tile set * tpg + ti.
+  // Consecutive groups hold the tile sets of one range, so all tiles of a
+  // range stream its pages at about the same time (the repeats come from
+  // L2).  When the tiles of a sequence divide the SM count, sets = 1 and a
+  // group holds every tile of its ranges.
+  const int tpg = P.tpg;
+  const int sets = kSets ? P.sets : 1;
+  const int ti = blockIdx.x % tpg;
+  const int gi = blockIdx.x / tpg;
+  const int NG = gridDim.x / tpg;
   const int TH = P.T * P.H;
   const int NS = P.num_slots;
   const uint32_t q_box_bytes = static_cast<uint32_t>(P.q_box_rows) * 128u;
@@ -225,7 +240,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const uint32_t q_bytes = q_box_bytes * kBoxes;
       int g = 0, pc = 0, nq = 0;  // nq: query-tile copies issued
       bool ok = true;
-      for (int k = k0; k < R && ok; k += G) {
+      for (int v = gi; v < R * sets && ok; v += NG) {
+        const int k = v / sets, tile = (v % sets) * tpg + ti;
         PieceWalker w(P, k);
         int b, pb, pe;
         while (ok && w.next(P, b, pb, pe)) {
@@ -338,8 +354,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const int qk_boxes = half == 0 ? 5 : 4;
       int g = 0, pc = 0;
       bool ok = true;
-      for (int k = k0; k < R && ok; k += G) {
-        PieceWalker w(P, k);
+      for (int v = gi; v < R * sets && ok; v += NG) {
+        PieceWalker w(P, v / sets);
         int b, pb, pe;
         while (ok && w.next(P, b, pb, pe)) {
           const ChunkRange cr(P.seq_len_eff[b], pb, pe);
@@ -427,7 +443,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const bool owner = par == 0;
     int g = 0, pc = 0;
     bool fail = false;
-    for (int k = k0; k < R && !fail; k += G) {
+    for (int v = gi; v < R * sets && !fail; v += NG) {
+      const int k = v / sets, tile = (v % sets) * tpg + ti;
       PieceWalker w(P, k);
       int b, pb, pe;
       while (!fail && w.next(P, b, pb, pe)) {
@@ -660,18 +677,49 @@ int decode_num_slots(int T, int H) {
 int decode_smem_bytes(int T, int H) {
   return 1024 + kBoxes * decode_q_box_rows(T, H) * 128 + decode_num_slots(T, H) * kSlotBytes;
 }
-// Largest number of co-resident CTA groups (one CTA per tile of a sequence's
-// query rows; one CTA per SM).
-cudaError_t decode_max_groups(int T, int H, int sm_count, int* groups) {
-  const int tiles = decode_tiles(T, H);
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       decode_smem_bytes(T, H));
+// How the attention step spreads over the SMs.  One CTA per SM and per
+// 64-row tile of a sequence's query rows.  When the tiles divide the SM
+// count, a CTA group holds all of them and there is one work range per group.
+// When they do not and the groups that fit would leave 3 % or more of the SMs
+// idle (16 tiles on 152 SMs: 9 groups, 8 SMs idle), a group holds
+// tpg = gcd(tiles, SMs) tiles instead, every SM gets a CTA, and the number of
+// ranges is the smallest that deals each group the same number of
+// (range, tile set) tasks.
+struct DecodeShape {
+  int tiles, tpg, sets, groups, ranges;
+};
+static int gcd_int(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+static DecodeShape decode_shape(int T, int H, int sm_count) {
+  DecodeShape d;
+  d.tiles = decode_tiles(T, H);
+  const int sms = sm_count > 0 ? sm_count : 1;
+  const int idle = d.tiles <= sms ? sms % d.tiles : 0;
+  d.tpg = (100 * idle >= 3 * sms) ? gcd_int(d.tiles, sms) : d.tiles;
+  d.sets = d.tiles / d.tpg;
+  d.groups = sms / d.tpg > 0 ? sms / d.tpg : 1;
+  d.ranges = d.groups / gcd_int(d.groups, d.sets);
+  return d;
+}
+
+// Default number of work ranges for the planner (see decode_shape).
+cudaError_t decode_default_ranges(int T, int H, int sm_count, int* ranges) {
+  const DecodeShape shape = decode_shape(T, H, sm_count);
+  cudaError_t e = cudaFuncSetAttribute(
+      shape.sets > 1 ? decode_kernel<true> : decode_kernel<false>,
+      cudaFuncAttributeMaxDynamicSharedMemorySize, decode_smem_bytes(T, H));
   if (e != cudaSuccess) return e;
-  *groups = sm_count / tiles > 0 ? sm_count / tiles : 1;
+  *ranges = shape.ranges;
   return cudaSuccess;
 }
 
-cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int groups,
+cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int sm_count,
                           const int32_t* block_table, const int32_t* seq_len_eff,
                           const PlanHeader* header, void* ws, const int32_t* seq_first,
                           const int32_t* seq_nsplit, const int32_t* seq_slot,
@@ -679,8 +727,9 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
                           int32_t* status, int B, int T, int H, int max_pages,
                           int num_pages, float scale, cudaStream_t st) {
   const int smem = decode_smem_bytes(T, H);
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem);
+  const DecodeShape shape = decode_shape(T, H, sm_count);
+  auto kern = shape.sets > 1 ? decode_kernel<true> : decode_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   DecodeParams P;
   P.block_table = block_table;
@@ -702,13 +751,14 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
   P.H = H;
   P.max_pages = max_pages;
   P.num_pages = num_pages;
-  P.tiles = decode_tiles(T, H);
+  P.tpg = shape.tpg;
+  P.sets = shape.sets;
   P.q_box_rows = decode_q_box_rows(T, H);
   P.num_slots = decode_num_slots(T, H);
   P.scale = scale;
   P.scale_log2 = scale * 1.4426950408889634f;
 
-  e = launch_pdl(decode_kernel, dim3(groups * P.tiles), dim3(kDecThreads), smem, st,
+  e = launch_pdl(kern, dim3(shape.groups * shape.tpg), dim3(kDecThreads), smem, st,
                  tm_q, tm_c, P);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -85,15 +85,39 @@ def test_tiny_workload_all_rows():
 
 
 # 48/80 heads leave a partial last tile; 96 x 2 rows make three tiles; 112 x 2
-# rows make four with a 32-row last tile.
+# rows make four with a 32-row last tile.  128 x 6, 112 x 8 and 128 x 8 rows
+# make 12, 14 and 16 tiles, which do not divide 152 SMs: CTA groups then hold
+# 4, 2 and 8 tiles and each takes several (range, tile set) tasks.
 @pytest.mark.parametrize("H,T", [(16, 1), (32, 1), (64, 1), (128, 1), (16, 2), (64, 2), (128, 2),
                                  (48, 1), (80, 1), (96, 2), (112, 2),
-                                 (16, 4), (128, 3), (64, 8), (128, 8)])
+                                 (16, 4), (128, 3), (64, 8), (128, 8), (128, 6), (112, 8)])
 def test_ragged_lengths_all_rows(H, T):
     lens = [T, 1 + T, 63, 64, 65, 127, 128, 129, 200, 511, 700]
     inp = make_inputs(len(lens), lens, T, H, seed=100 + H + T)
     out, lse, _ = run_gpu(inp)
     assert_parity(compare(inp, out, lse), "H=%d T=%d" % (H, T))
+
+
+def default_ranges_expected(T, H, sms):
+    """The attention step's default work-range count: one per CTA group of
+    all a sequence's 64-row tiles when those groups fill the SMs to within 3 %;
+    otherwise groups of gcd(tiles, SMs) tiles, and the fewest ranges that deal
+    every group the same number of (range, tile set) tasks."""
+    tiles = -(-T * H // 64)
+    idle = sms % tiles
+    tpg = math.gcd(tiles, sms) if 100 * idle >= 3 * sms else tiles
+    groups, sets = sms // tpg, tiles // tpg
+    return groups // math.gcd(groups, sets)
+
+
+@pytest.mark.parametrize("T,H", [(1, 16), (1, 128), (2, 128), (6, 128), (7, 128), (8, 128),
+                                 (8, 112), (3, 128)])
+def test_default_range_count(T, H):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    inp = make_inputs(3, [T + 100, T + 700, T + 2000], T, H, seed=44)
+    out, lse, m = run_gpu(inp)
+    assert m.plan_header()[0] == default_ranges_expected(T, H, sms)
+    assert_parity(compare(inp, out, lse), "default ranges T=%d H=%d" % (T, H))
 
 
 @pytest.mark.parametrize("num_ranges", [1, 3, 7, 64, 300, 1000])
