@@ -260,10 +260,11 @@ int mla_decode_run_static_scratch(const mla_decode_dims* dims, const void* q,
 
 /* Number of kernels one whole run enqueues (launch accounting; the plan is
  * not counted): *kernels = 4 (absorb, attention, combine, up-projection), or
- * 3 when mla_decode_run (bf16 weights, fp8_weights = 0) takes the fused
- * combine + up-projection of small batches: fewer than 128 tokens
- * (batch x q_len) whose 16-token tiles of all heads fit in one wave on the
- * device's SMs.  The count depends on the current device's SM count.
+ * 3 when the run (mla_decode_run, or mla_decode_run_fp8w: fp8_weights
+ * nonzero; the count is the same) takes the fused combine + up-projection of
+ * small batches: fewer than 128 tokens (batch x q_len) whose 16-token tiles
+ * of all heads fit in one wave on the device's SMs.  The count depends on the
+ * current device's SM count.
  * Returns MLA_DECODE_INVALID_ARG for bad dims or a null `kernels`, before any
  * device query; MLA_DECODE_CUDA_ERROR if the device cannot be queried. */
 int mla_decode_kernels_per_run(const mla_decode_dims* d, int32_t fp8_weights, int32_t* kernels);

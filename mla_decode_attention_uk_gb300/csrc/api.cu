@@ -54,7 +54,7 @@ cudaError_t launch_combine_up(const CUtensorMap& tm_wuv, int B, int T, int H, co
                               const int32_t* seq_slot, const uint8_t* qlo,
                               const __nv_bfloat16* olat, float* lse, float scale,
                               __nv_bfloat16* out, int32_t* status, int splits_per_seq,
-                              cudaStream_t st);
+                              const float* wuv_scale, cudaStream_t st);
 }  // namespace mla
 
 namespace {
@@ -510,9 +510,9 @@ static int combine_impl(const mla_decode_dims* d, float scale, float* lse, void*
                                 at<int32_t>(ws, L.status), static_cast<cudaStream_t>(stream)));
 }
 
-// Whether a whole run with bf16 weights merges the splits inside the
-// up-projection (combine_up_kernel): fewer than 128 tokens, in 16-token tiles
-// of every head that fit in one wave on the SMs.
+// Whether a whole run merges the splits inside the up-projection
+// (combine_up_kernel): fewer than 128 tokens, in 16-token tiles of every head
+// that fit in one wave on the SMs.
 static int run_uses_combine_up(const mla_decode_dims* d, bool* fused) {
   int sms = 0;
   const int rc = sm_count(&sms);
@@ -522,10 +522,12 @@ static int run_uses_combine_up(const mla_decode_dims* d, bool* fused) {
   return MLA_DECODE_OK;
 }
 
-// Combine and up-projection of such a run in one launch; out and lse equal
-// those of mla_decode_combine followed by mla_decode_up_project bit for bit.
-static int combine_up_impl(const mla_decode_dims* d, const void* w_uv, float scale, void* out,
-                           float* lse, void* ws, size_t ws_bytes, void* stream) {
+// Combine and up-projection of such a run in one launch, with bf16 weights
+// (w_uv) or FP8 weights (w8 with block scales); out and lse equal those of the
+// combine step followed by the up-projection step bit for bit.
+static int combine_up_impl(const mla_decode_dims* d, const void* w_uv, const uint8_t* w8,
+                           const float* w8_scale, float scale, void* out, float* lse, void* ws,
+                           size_t ws_bytes, void* stream) {
   WsLayout L;
   int rc = layout_for(d, ws_bytes, &L);
   if (rc) return rc;
@@ -533,14 +535,16 @@ static int combine_up_impl(const mla_decode_dims* d, const void* w_uv, float sca
   rc = combine_variant(d, &ranges, &splits_per_seq);
   if (rc) return rc;
   CUtensorMap tm_w;
-  if (!make_map(&tm_w, w_uv, static_cast<uint64_t>(d->num_heads) * kLora, kVHead, kVHead,
-                kBoxCols, 64, false))
+  const uint64_t wrows = static_cast<uint64_t>(d->num_heads) * kLora;
+  if (!(w8 ? make_map(&tm_w, w8, wrows, kVHead, kVHead, 128, 64, false, 1)
+           : make_map(&tm_w, w_uv, wrows, kVHead, kVHead, kBoxCols, 64, false)))
     return MLA_DECODE_CUDA_ERROR;
   return cuda_rc(launch_combine_up(
       tm_w, d->batch, d->q_len, d->num_heads, ws, at<PlanHeader>(ws, L.header),
       at<int32_t>(ws, L.seq_nsplit), at<int32_t>(ws, L.seq_slot), at<uint8_t>(ws, L.qlo),
       at<__nv_bfloat16>(ws, L.olat), lse, scale, static_cast<__nv_bfloat16*>(out),
-      at<int32_t>(ws, L.status), splits_per_seq, static_cast<cudaStream_t>(stream)));
+      at<int32_t>(ws, L.status), splits_per_seq, w8 ? w8_scale : nullptr,
+      static_cast<cudaStream_t>(stream)));
 }
 
 int mla_decode_combine(const mla_decode_dims* d, float scale, float* lse, void* ws,
@@ -592,7 +596,8 @@ int mla_decode_run(const mla_decode_dims* d, const void* q, const void* kv_cache
   bool fused = false;
   rc = run_uses_combine_up(d, &fused);
   if (rc) return rc;
-  if (fused) return combine_up_impl(d, w_uv, scale, out, lse, ws, ws_bytes, stream);
+  if (fused)
+    return combine_up_impl(d, w_uv, nullptr, nullptr, scale, out, lse, ws, ws_bytes, stream);
   // Large batches: the combine merges split sequences only and the
   // up-projection corrects the lse of the others from the o_lat and q_lo
   // tiles it stages anyway (one read of each instead of two).
@@ -619,7 +624,13 @@ int mla_decode_run_fp8w(const mla_decode_dims* d, const void* q, const void* kv_
   if (rc) return rc;
   rc = mla_decode_attend(d, kv_cache, block_table, seq_lens, scale, lse, ws, ws_bytes, stream);
   if (rc) return rc;
-  bool rows = false;  // as in mla_decode_run
+  bool fused = false;  // as in mla_decode_run
+  rc = run_uses_combine_up(d, &fused);
+  if (rc) return rc;
+  if (fused)
+    return combine_up_impl(d, nullptr, w_uv_fp8, w_uv_scale, scale, out, lse, ws, ws_bytes,
+                           stream);
+  bool rows = false;
   rc = run_uses_up_rows(d, &rows);
   if (rc) return rc;
   rc = combine_impl(d, scale, lse, ws, ws_bytes, stream, rows);
@@ -635,11 +646,10 @@ int mla_decode_kernels_per_run(const mla_decode_dims* d, int32_t fp8_weights,
   int rc = check_dims(d);
   if (rc) return rc;
   if (!kernels) return MLA_DECODE_INVALID_ARG;
+  (void)fp8_weights;  // both weight formats take the same arrangement
   bool fused = false;
-  if (!fp8_weights) {
-    rc = run_uses_combine_up(d, &fused);
-    if (rc) return rc;
-  }
+  rc = run_uses_combine_up(d, &fused);
+  if (rc) return rc;
   *kernels = fused ? 3 : 4;
   return MLA_DECODE_OK;
 }

@@ -1047,21 +1047,31 @@ up_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
 // by TMA before the wait for the attention step.
 //   warp 0: TMA producer; warp 1: MMA issuer; warp 2: TMEM owner; warps 0-3:
 //   epilogue (as in bmm_kernel); warps 4-19: merge warps.
+// FP8 weights (W8): the eight raw 64 k x 128 m FP8 slices load instead, and
+// warps 20-23 decompress each into its bf16 stage (convert_fp8_row, the
+// layout TMA gives the bf16 slices), so the result equals the bf16 weights'
+// run on the decompressed weights bit for bit.
 constexpr int kCuNT = 16;                            // tokens per tile
 constexpr int kCuThreads = 128 + 32 * kCuNT;
 constexpr int kCuChunkBytes = kCuNT * 128;           // one 64-deep K chunk of the B tile
 constexpr int kCuSmem = 8 * kABytes + 8 * kCuChunkBytes + 1024;
 
-template <int kUnroll, int kFewN>
-__global__ void __launch_bounds__(kCuThreads, 1)
+template <bool W8>
+struct CuCfg {
+  static constexpr int kThreads = kCuThreads + (W8 ? 128 : 0);
+  static constexpr int kSmem = kCuSmem + (W8 ? 8 * kRawBytes : 0);
+};
+
+template <int kUnroll, int kFewN, bool W8>
+__global__ void __launch_bounds__(CuCfg<W8>::kThreads, 1)
 combine_up_kernel(const __grid_constant__ CUtensorMap tm_w, int B, int T, int H,
                   const uint8_t* __restrict__ ws, const PlanHeader* __restrict__ header,
                   const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict__ seq_slot,
                   const uint8_t* __restrict__ qlo, const __nv_bfloat16* __restrict__ olat,
                   float* __restrict__ lse, float scale, __nv_bfloat16* __restrict__ out,
-                  int32_t* __restrict__ status) {
+                  int32_t* __restrict__ status, const float* __restrict__ w8_scale) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[8], b_ready, done_bar;
+  __shared__ __align__(8) uint64_t full_bar[8], conv_bar[W8 ? 8 : 1], b_ready, done_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -1073,9 +1083,12 @@ combine_up_kernel(const __grid_constant__ CUtensorMap tm_w, int B, int T, int H,
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const sbase_ptr = smem_raw + (sbase - smem_u32(smem_raw));
   const uint32_t btile = sbase + 8 * kABytes;
+  const uint32_t rawbase = btile + 8 * kCuChunkBytes;  // W8: raw FP8 slices
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 8; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
+    if constexpr (W8)
+      for (int s = 0; s < 8; ++s) mbar_init(smem_u32(&conv_bar[s]), 1);
     mbar_init(smem_u32(&b_ready), 1);
     mbar_init(smem_u32(&done_bar), 1);
     abort_sh = 0;
@@ -1097,9 +1110,14 @@ combine_up_kernel(const __grid_constant__ CUtensorMap tm_w, int B, int T, int H,
       for (int kc = 0; kc < 8; ++kc) {
         const uint32_t a = sbase + kc * kABytes;
         const uint32_t fb = smem_u32(&full_bar[kc]);
-        mbar_expect_tx(fb, kABytes);
-        tma_load_2d(a, &tm_w, 0, h * kLora + kc * 64, fb);
-        tma_load_2d(a + kBoxBytes, &tm_w, 64, h * kLora + kc * 64, fb);
+        if constexpr (W8) {
+          mbar_expect_tx(fb, kRawBytes);
+          tma_load_2d(rawbase + kc * kRawBytes, &tm_w, 0, h * kLora + kc * 64, fb);
+        } else {
+          mbar_expect_tx(fb, kABytes);
+          tma_load_2d(a, &tm_w, 0, h * kLora + kc * 64, fb);
+          tma_load_2d(a + kBoxBytes, &tm_w, 64, h * kLora + kc * 64, fb);
+        }
       }
     }
   } else if (warp == 1) {
@@ -1108,6 +1126,7 @@ combine_up_kernel(const __grid_constant__ CUtensorMap tm_w, int B, int T, int H,
       if (mbar_wait(smem_u32(&b_ready), 0, &abort_sh, status)) {
         for (int kc = 0; kc < 8; ++kc) {
           if (!mbar_wait(smem_u32(&full_bar[kc]), 0, &abort_sh, status)) break;
+          if (W8 && !mbar_wait(smem_u32(&conv_bar[kc]), 0, &abort_sh, status)) break;
           tc_fence_after();
           const uint32_t a = sbase + kc * kABytes;
           const uint32_t b = btile + kc * kCuChunkBytes;
@@ -1120,6 +1139,20 @@ combine_up_kernel(const __grid_constant__ CUtensorMap tm_w, int B, int T, int H,
         }
       }
       umma_commit(smem_u32(&done_bar));
+    }
+  } else if (W8 && warp >= 4 + kCuNT) {
+    // FP8 converters: thread ct owns k row ct / 2, columns 64 (ct % 2) .. + 63
+    // of each slice; W_UV's scales [H, 4, 1] hold one per 128 k rows.
+    const int ct = threadIdx.x - kCuThreads;
+    bool ok = true;
+    for (int kc = 0; kc < 8; ++kc) {
+      ok = mbar_wait(smem_u32(&full_bar[kc]), 0, &abort_sh, status);
+      if (!named_bar_and(3, 128, ok)) break;
+      const float sc = __ldg(w8_scale + h * (kLora / 128) + kc / 2);
+      convert_fp8_row(rawbase + kc * kRawBytes, sbase + kc * kABytes, ct >> 1, ct & 1, sc);
+      fence_proxy_async_smem();  // the bf16 slice goes to the tensor core
+      named_bar_sync(3, 128);
+      if (ct == 0) mbar_arrive(smem_u32(&conv_bar[kc]));
     }
   } else if (warp >= 4) {
     // Merge warp mw: token tok0 + mw, row mw of each K chunk of the B tile
@@ -1260,19 +1293,20 @@ cudaError_t launch_up_rows(const CUtensorMap& tw, const CUtensorMap& to, const C
   return cudaGetLastError();
 }
 
-template <int kUnroll, int kFewN>
+template <int kUnroll, int kFewN, bool W8>
 cudaError_t launch_cu(const CUtensorMap& tw, int B, int T, int H, const void* ws,
                       const PlanHeader* header, const int32_t* seq_nsplit,
                       const int32_t* seq_slot, const uint8_t* qlo, const __nv_bfloat16* olat,
                       float* lse, float scale, __nv_bfloat16* out, int32_t* status,
-                      cudaStream_t st) {
-  auto kern = combine_up_kernel<kUnroll, kFewN>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCuSmem);
+                      const float* w8_scale, cudaStream_t st) {
+  using C = CuCfg<W8>;
+  auto kern = combine_up_kernel<kUnroll, kFewN, W8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((B * T + kCuNT - 1) / kCuNT, H);
-  e = launch_pdl(kern, grid, dim3(kCuThreads), kCuSmem, st, tw, B, T, H,
+  e = launch_pdl(kern, grid, dim3(C::kThreads), C::kSmem, st, tw, B, T, H,
                  static_cast<const uint8_t*>(ws), header, seq_nsplit, seq_slot, qlo, olat, lse,
-                 scale, out, status);
+                 scale, out, status, w8_scale);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1352,24 +1386,26 @@ cudaError_t launch_up_project_rows(const CUtensorMap& tm_wuv, const CUtensorMap&
                                            lse, scale, status, nullptr, sm_count, st);
 }
 
-// Small one-wave batches: combine and up-projection in one kernel
-// (bf16 weights).  splits_per_seq picks the same merge variant as the
-// combine step would.
+// Small one-wave batches: combine and up-projection in one kernel, with
+// bf16 weights (tm_wuv over w_uv) or FP8 weights (tm_wuv over the FP8 codes,
+// wuv_scale their block scales).  splits_per_seq picks the same merge
+// variant as the combine step would.
 int combine_up_tile() { return kCuNT; }
 cudaError_t launch_combine_up(const CUtensorMap& tm_wuv, int B, int T, int H, const void* ws,
                               const PlanHeader* header, const int32_t* seq_nsplit,
                               const int32_t* seq_slot, const uint8_t* qlo,
                               const __nv_bfloat16* olat, float* lse, float scale,
                               __nv_bfloat16* out, int32_t* status, int splits_per_seq,
-                              cudaStream_t st) {
-  if (splits_per_seq <= 1)
-    return launch_cu<1, 2>(tm_wuv, B, T, H, ws, header, seq_nsplit, seq_slot, qlo, olat, lse,
-                           scale, out, status, st);
-  if (splits_per_seq <= 4)
-    return launch_cu<4, 4>(tm_wuv, B, T, H, ws, header, seq_nsplit, seq_slot, qlo, olat, lse,
-                           scale, out, status, st);
-  return launch_cu<4, 0>(tm_wuv, B, T, H, ws, header, seq_nsplit, seq_slot, qlo, olat, lse, scale,
-                         out, status, st);
+                              const float* wuv_scale, cudaStream_t st) {
+#define MLA_CU_LAUNCH(U, F)                                                                      \
+  (wuv_scale ? launch_cu<U, F, true>(tm_wuv, B, T, H, ws, header, seq_nsplit, seq_slot, qlo,    \
+                                     olat, lse, scale, out, status, wuv_scale, st)             \
+             : launch_cu<U, F, false>(tm_wuv, B, T, H, ws, header, seq_nsplit, seq_slot, qlo,   \
+                                      olat, lse, scale, out, status, nullptr, st))
+  if (splits_per_seq <= 1) return MLA_CU_LAUNCH(1, 2);
+  if (splits_per_seq <= 4) return MLA_CU_LAUNCH(4, 4);
+  return MLA_CU_LAUNCH(4, 0);
+#undef MLA_CU_LAUNCH
 }
 
 }  // namespace mla
