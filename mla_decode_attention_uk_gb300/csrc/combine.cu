@@ -78,10 +78,10 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
 // unsplit rows itself.  Sequence b is split exactly when a work range starts
 // inside it, and the first such range is k = seq_first[b] + 1, so walking the
 // ranges visits every split sequence once; the grid's y dimension strides
-// over them and its x dimension over blocks of kSplitRows rows.  A CTA that
+// over them and its x dimension over blocks of rows_blk rows.  A CTA that
 // finds a split sequence brings the partial rows of its row block into
 // shared memory with one bulk copy per split (the rows of one split are
-// contiguous: 16 x 1 KB), so all of a block's partials are in flight at once
+// contiguous: rows_blk x 1 KB), so all of a block's partials are in flight at once
 // instead of the few that one warp per row keeps in registers (measured:
 // that form cost 11.7 us of a 512-token x 128-head step, latency-bound at
 // one or two CTAs per SM).  Sequences with more splits than are staged read
@@ -90,7 +90,7 @@ combine_kernel(const int32_t* __restrict__ seq_nsplit, const int32_t* __restrict
 // instantiations registers; its grid is small, so it may use what it
 // needs: two CTAs per SM, one for the variant that keeps four splits'
 // partials in registers.)
-constexpr int kSplitRows = 16;
+
 
 template <int kUnroll, int kFewN>
 __global__ void __launch_bounds__(kCombThreads, kFewN == 4 ? 1 : 2)
@@ -99,15 +99,15 @@ combine_split_kernel(const int32_t* __restrict__ seq_nsplit,
                      const PlanHeader* __restrict__ header, int B, int T, int H,
                      const uint8_t* __restrict__ qlo, __nv_bfloat16* __restrict__ olat,
                      float* __restrict__ lse_out, float scale, int stage_splits,
-                     int32_t* __restrict__ status) {
+                     int rows_blk, int32_t* __restrict__ status) {
   extern __shared__ __align__(128) uint8_t stage_raw[];
   __shared__ __align__(8) uint64_t full_bar;
   __shared__ int abort_sh;
   // The plan is complete when this kernel starts (as in combine_kernel).
   griddep_launch_dependents();
   const int TH = T * H;
-  const int r0 = blockIdx.x * kSplitRows;
-  const int nrows = min(kSplitRows, TH - r0);
+  const int r0 = blockIdx.x * rows_blk;
+  const int nrows = min(rows_blk, TH - r0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&full_bar), 1);
@@ -137,7 +137,7 @@ combine_split_kernel(const int32_t* __restrict__ seq_nsplit,
         const uint32_t bytes = static_cast<uint32_t>(nrows) * kLora * 2;
         mbar_expect_tx(smem_u32(&full_bar), bytes * ns);
         for (int s = 0; s < ns; ++s)
-          bulk_load_g2s(smem_u32(stage_raw) + s * kSplitRows * kLora * 2,
+          bulk_load_g2s(smem_u32(stage_raw) + s * rows_blk * kLora * 2,
                         opart + (static_cast<size_t>(slot0 + s) * TH + r0) * kLora, bytes,
                         smem_u32(&full_bar));
         ++issued;
@@ -156,7 +156,7 @@ combine_split_kernel(const int32_t* __restrict__ seq_nsplit,
           merge_split_row<kUnroll, kFewN>(
               b, r, lane, ns, slot0, B, T, H, ws, header, qlo, lse_out, scale, sink,
               [&](const __nv_bfloat16*, int, int s, int, int) {
-                return stage + (s * kSplitRows + rr) * (kLora / 4);
+                return stage + (s * rows_blk + rr) * (kLora / 4);
               });
         } else {
           merge_split_row<kUnroll, kFewN>(b, r, lane, ns, slot0, B, T, H, ws, header, qlo,
@@ -188,17 +188,24 @@ cudaError_t launch_combine(const int32_t* seq_nsplit, const int32_t* seq_slot, c
     // Split sequences only, the grid's y dimension striding over that many
     // work ranges (the planner's count or any other); partials of up to
     // stage_splits splits are staged in shared memory.
-    const int stage_splits = splits_per_seq <= 1 ? 4 : (splits_per_seq <= 4 ? 8 : 12);
-    const int smem = stage_splits * kSplitRows * kLora * 2;
+    // Blocks of 16 rows, or 32 when 16-row blocks over every range would
+    // take more than two waves of CTAs (608 = two waves of two CTAs on each of
+    // 152 SMs, the count this was tuned on; elsewhere only the speed
+    // changes).  Measured: 1024 query rows x 18 ranges, step 487.0 -> 484.2
+    // us with 32-row blocks; 256 x 37 (592 CTAs) lost 2.9 us with them.
+    const int rows_blk = (T * H + 15) / 16 * split_ranges > 608 ? 32 : 16;
+    const int stage_splits =
+        (splits_per_seq <= 1 ? 2 : (splits_per_seq <= 4 ? 4 : 6)) * (32 / rows_blk);
+    const int smem = stage_splits * rows_blk * kLora * 2;
     auto kern = splits_per_seq <= 1   ? combine_split_kernel<1, 2>
                 : splits_per_seq <= 4 ? combine_split_kernel<4, 4>
                                       : combine_split_kernel<4, 0>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((T * H + kSplitRows - 1) / kSplitRows, split_ranges);
+    dim3 grid((T * H + rows_blk - 1) / rows_blk, split_ranges);
     e = launch_pdl(kern, grid, dim3(kCombThreads), smem, st, seq_nsplit, seq_slot,
                    static_cast<const uint8_t*>(ws), header, B, T, H, qlo, olat, lse, scale,
-                   stage_splits, status);
+                   stage_splits, rows_blk, status);
   } else {
     auto kern = splits_per_seq <= 1   ? combine_kernel<1, 2>
                 : splits_per_seq <= 4 ? combine_kernel<4, 4>
