@@ -66,7 +66,7 @@ constexpr uint64_t kLoadOrder = 0x876325410ull;    // 0, 1, 4, 5, 2, 3, 6, 7, 8
 constexpr uint64_t kQkOrder0 = 0x32410ull;         // 0, 1, 4, 2, 3
 constexpr uint64_t kQkOrder1 = 0x8765ull;          // 5, 6, 7, 8
 __host__ __device__ constexpr int free_group(int box) { return box == kRopeBox ? 4 : box >> 1; }
-constexpr int kPrefetchPages = 2;                  // L2 prefetch distance, in pages
+constexpr int kPrefetchPages = 2;                  // L2 prefetch distance, in pages (at most)
 constexpr int kDynSmemMax = 232448 - 2048;         // opt-in limit minus static smem budget
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;                   // O^T blocks at 256 + 64 m
@@ -90,6 +90,7 @@ struct DecodeParams {
   int32_t* status;
   int B, T, H, max_pages, num_pages, q_box_rows, num_slots;
   int tpg, sets;             // tiles per CTA group; tile sets per sequence
+  int pf_near;               // L2 prefetch one page ahead instead of kPrefetchPages
   float scale, scale_log2;
 };
 
@@ -256,9 +257,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           ++nq;
           const ChunkRange cr(P.seq_len_eff[b], pb, pe);
           const int32_t* bt_row = P.block_table + static_cast<size_t>(b) * P.max_pages;
-          // Pages are also prefetched into L2 kPrefetchPages ahead of their
-          // shared-memory load, so a slot refill mostly hits L2 instead of
-          // waiting a full HBM round trip.
+          // Pages are also prefetched into L2 ahead of their shared-memory
+          // load, so a slot refill mostly hits L2 instead of waiting a full
+          // HBM round trip: kPrefetchPages ahead, or one page when a
+          // sequence's rows fit one CTA (P.pf_near; each page is then read
+          // by one CTA only, and the nearer prefetch measured 1.9 % faster on
+          // 16 heads, the farther one 0.2-0.6 % faster where two or more
+          // tiles share each page).
           auto page_of = [&](int i) {
             int pg = __ldg(bt_row + cr.page(i));
             if (pg < 0 || pg >= P.num_pages) {
@@ -274,7 +279,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
           for (int a = 0; a < kLookAhead; ++a) {
             ahead[a] = a < cr.nchunks ? page_of(a) : 0;
-            if (kPrefetchPages > 0 && a < cr.nchunks)
+            if (kPrefetchPages > 0 && a < cr.nchunks && (a == 0 || !P.pf_near))
               for (int j = 0; j < kBoxes; ++j)
                 tma_prefetch_l2_2d(&tm_c, j * kBoxCols, ahead[a] * kPage);
           }
@@ -312,9 +317,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             for (int a = 0; a + 1 < kLookAhead; ++a) ahead[a] = ahead[a + 1];
             const int nxt = i + kLookAhead;
             ahead[kLookAhead - 1] = nxt < cr.nchunks ? page_of(nxt) : 0;
-            if (kPrefetchPages > 0 && nxt < cr.nchunks)
+            // The page to prefetch: i + kLookAhead, or i + 1 (near).
+            const int pf = P.pf_near ? i + 1 : nxt;
+            if (kPrefetchPages > 0 && pf < cr.nchunks)
               for (int j = 0; j < kBoxes; ++j)
-                tma_prefetch_l2_2d(&tm_c, j * kBoxCols, ahead[kLookAhead - 1] * kPage);
+                tma_prefetch_l2_2d(&tm_c, j * kBoxCols,
+                                   (P.pf_near ? ahead[0] : ahead[kLookAhead - 1]) * kPage);
           }
           ++pc;
         }
@@ -753,6 +761,7 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_c, int 
   P.num_pages = num_pages;
   P.tpg = shape.tpg;
   P.sets = shape.sets;
+  P.pf_near = shape.tiles == 1 ? 1 : 0;
   P.q_box_rows = decode_q_box_rows(T, H);
   P.num_slots = decode_num_slots(T, H);
   P.scale = scale;
