@@ -278,6 +278,34 @@ def test_large_run_matches_step_calls(R):
     assert_parity(compare(inp, o1.cpu(), l1.cpu()), "large run R=%d" % R)
 
 
+def test_large_run_ragged_split_blocks():
+    # 400 tokens x 48 heads: 4 token tiles x 48 heads = 192 units of 128
+    # tokens x one head, more than the SMs, so the large-run path.  300 ranges make
+    # the split-only combine use 32-row blocks, and 48 rows per sequence
+    # leave a 16-row last block.  out bit for bit as the step calls, lse up
+    # to the summation order of the correction, every row against the oracle.
+    g = torch.Generator().manual_seed(93)
+    lens = torch.randint(1, 300, (400,), generator=g).tolist()
+    inp = make_inputs(400, lens, 1, 48, seed=94)
+    dev = torch.device("cuda")
+    gd = inp.to(dev)
+    m = binding.MlaDecode(binding.dims_for(gd.q, gd.cache, gd.block_table), dev, 300)
+    o1 = torch.empty(400, 1, 48, 128, dtype=torch.bfloat16, device=dev)
+    l1 = torch.empty(400, 1, 48, dtype=torch.float32, device=dev)
+    o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
+    m.plan(gd.seq_lens)
+    m.run(gd.q, gd.cache, gd.block_table, gd.seq_lens, gd.w_uk, gd.w_uv, gd.scale, o1, l1)
+    m.plan(gd.seq_lens)
+    m.absorb(gd.q, gd.w_uk)
+    m.attend(gd.cache, gd.block_table, gd.seq_lens, gd.scale, l2)
+    m.combine(gd.scale, l2)
+    m.up_project(gd.w_uv, o2)
+    assert m.check() == 0
+    assert torch.equal(o1, o2)
+    assert (l1 - l2).abs().max().item() <= 1e-6
+    assert_parity(compare(inp, o1.cpu(), l1.cpu()), "large run, ragged 32-row split blocks")
+
+
 def test_page_permutation_same_schedule_bitwise():
     inp = make_inputs(3, [130, 640, 77], 1, 32, seed=10)
     o1, l1, _ = run_gpu(inp)
