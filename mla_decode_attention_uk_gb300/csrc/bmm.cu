@@ -1038,8 +1038,9 @@ up_rows_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__
 // Combine and up-projection in one kernel, for small batches whose
 // 16-token tiles of all heads fit in one wave: the up-projection's B operand
 // (the tile's o rows, bf16) is built in shared memory by merge warps, one per
-// token, with the combine's own routines (merge.cuh), so o_lat never goes
-// through global memory and one kernel boundary of the step disappears.
+// token, with the combine's own routines (merge.cuh), so a merged row never
+// goes through global memory (unsplit rows are read from o_lat as the
+// attention step wrote them) and one kernel boundary of the step disappears.
 // Rows of split sequences are merged from their partials, rows of unsplit
 // ones copied from o_lat; either way the row's lse gets its first-order
 // correction, and the result equals, bit for bit, the combine kernel followed
