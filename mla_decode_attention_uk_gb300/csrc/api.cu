@@ -391,7 +391,9 @@ static int up_project_impl(const mla_decode_dims* d, const void* w_uv, const uin
 // unsplit sequences (then the combine merges split sequences only): 128
 // tokens or more, in more (128-token tile, head) units than there are SMs.
 // Measured: 512 tokens x 128 heads (512 units), step 319.3 -> 314.8 us; 128
-// tokens x 128 heads (128 units on 152 SMs, one per SM), 235.4 -> 236.8 us.
+// tokens x 128 heads (128 units on 152 SMs, one per SM), 235.4 -> 236.8 us,
+// and still 227.6 -> 231.2 us once the split-only combine staged bf16
+// partials.
 static int run_uses_up_rows(const mla_decode_dims* d, bool* rows) {
   int sms = 0;
   const int rc = sm_count(&sms);
