@@ -534,13 +534,25 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             l = l * alpha + sum;
             if (owner) alpha_sh[srow_c] = alpha;
             // Pair up neighbouring keys: the even-key thread writes keys 0..31
-            // of the chunk, the odd-key thread keys 32..63.
+            // of the chunk, the odd-key thread keys 32..63.  The values cross
+            // to the partner already rounded to bf16, two per shuffle (8
+            // shuffles instead of 16: the shuffles queue behind the tensor
+            // core's shared-memory reads), and byte permutes form the pairs.
             uint32_t packed[16];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              const float send = par ? p[q] : p[16 + q];
-              const float recv = __shfl_xor_sync(0xffffffffu, send, 2);
-              packed[q] = par ? pack_bf16x2(recv, p[16 + q]) : pack_bf16x2(p[q], recv);
+            for (int k = 0; k < 8; ++k) {
+              // Sent: p[2k], p[2k+1] (odd thread) or p[16+2k], p[16+2k+1]
+              // (even thread); kept: the other half.
+              const uint32_t first = pack_bf16x2(p[2 * k], p[2 * k + 1]);
+              const uint32_t second = pack_bf16x2(p[16 + 2 * k], p[16 + 2 * k + 1]);
+              const uint32_t send2 = par ? first : second;
+              const uint32_t own2 = par ? second : first;
+              const uint32_t recv2 = __shfl_xor_sync(0xffffffffu, send2, 2);
+              // Even thread: (own key, partner key); odd thread: (partner,
+              // own).  Low halves give pair 2k, high halves pair 2k + 1.
+              const uint32_t lo_a = par ? recv2 : own2, lo_b = par ? own2 : recv2;
+              packed[2 * k] = __byte_perm(lo_a, lo_b, 0x5410);
+              packed[2 * k + 1] = __byte_perm(lo_a, lo_b, 0x7632);
             }
             // P^T goes into the page's RoPE box: QK^T, its only reader, is
             // complete (S is), and the box is not refilled before PV is done.
