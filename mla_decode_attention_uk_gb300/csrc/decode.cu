@@ -117,11 +117,14 @@ __device__ __forceinline__ bool bar_any(uint32_t id, uint32_t n, bool pred) {
 // Walks the pieces (sequence, page range) of work range k.
 struct PieceWalker {
   int b, p, b1, p1;
+  __device__ PieceWalker() : b(0), p(0), b1(0), p1(0) {}  // no pieces
   __device__ PieceWalker(const DecodeParams& P, int k)
       : b(P.range_b[k]), p(P.range_p[k]), b1(P.range_b[k + 1]), p1(P.range_p[k + 1]) {}
-  __device__ bool next(const DecodeParams& P, int& pb, int& pbeg, int& pend) {
+  // len: the piece's sequence length (seq_len_eff), read on the way.
+  __device__ bool next(const DecodeParams& P, int& pb, int& pbeg, int& pend, int& len) {
     while (b < b1 || (b == b1 && p < p1)) {
-      const int pages = (P.seq_len_eff[b] + kPage - 1) / kPage;
+      const int L = P.seq_len_eff[b];
+      const int pages = (L + kPage - 1) / kPage;
       const int e = (b == b1) ? p1 : pages;
       const int cb = b, cp = p;
       b += 1;
@@ -130,8 +133,35 @@ struct PieceWalker {
         pb = cb;
         pbeg = cp;
         pend = e;
+        len = L;
         return true;
       }
+    }
+    return false;
+  }
+  __device__ bool next(const DecodeParams& P, int& pb, int& pbeg, int& pend) {
+    int len;
+    return next(P, pb, pbeg, pend, len);
+  }
+};
+
+// Every piece of a CTA's tasks v = v0, v0 + stride, ... < nv in order (the
+// order all roles walk), for a role that wants to find its next piece early.
+struct PieceStream {
+  int v, stride, nv, sets;
+  PieceWalker w;
+  __device__ PieceStream(const DecodeParams& P, int v0, int stride_, int nv_, int sets_)
+      : v(v0), stride(stride_), nv(nv_), sets(sets_),
+        w(v0 < nv_ ? PieceWalker(P, v0 / sets_) : PieceWalker()) {}
+  __device__ bool next(const DecodeParams& P, int& task, int& pb, int& pbeg, int& pend,
+                       int& len) {
+    while (v < nv) {
+      if (w.next(P, pb, pbeg, pend, len)) {
+        task = v;
+        return true;
+      }
+      v += stride;
+      if (v < nv) w = PieceWalker(P, v / sets);
     }
     return false;
   }
@@ -451,14 +481,18 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const bool owner = par == 0;
     int g = 0, pc = 0;
     bool fail = false;
-    for (int v = gi; v < R * sets && !fail; v += NG) {
-      const int k = v / sets, tile = (v % sets) * tpg + ti;
-      PieceWalker w(P, k);
-      int b, pb, pe;
-      while (!fail && w.next(P, b, pb, pe)) {
+    // The next piece (and its sequence length) is found before the epilogue
+    // of the current one waits for the last PV, so those dependent global
+    // loads are off the path from the epilogue to the next piece's first
+    // softmax.
+    PieceStream ps(P, gi, NG, R * sets, sets);
+    int task, b, pb, pe, L;
+    bool have = ps.next(P, task, b, pb, pe, L);
+    while (!fail && have) {
+      {
+        const int k = task / sets, tile = (task % sets) * tpg + ti;
         const int r = tile * kTileRows + srow_c;  // row within the sequence's T*H rows
         const bool row_ok = r < TH;
-        const int L = P.seq_len_eff[b];
         // The epilogue's bookkeeping is loaded now, so that its memory round
         // trip is not on the path from the piece's last PV to the next
         // piece's first softmax.
@@ -611,6 +645,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           if (threadIdx.x == 128) mbar_arrive(smem_u32(&p_full[g % NS]));
         }
         if (fail) break;
+        const int cur_b = b;
+        have = ps.next(P, task, b, pb, pe, L);
 
         // ---------------- epilogue for this piece
         bool bad = !mbar_wait(smem_u32(&o_full), pc & 1, &abort_sh, P.status);
@@ -618,7 +654,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (owner) inv_l_sh[srow_c] = (row_ok && l > 0.0f) ? 1.0f / l : 0.0f;
         if (bar_any(1, 128, bad)) { fail = true; break; }
         tc_fence_after();
-        const size_t row_base = static_cast<size_t>(b) * TH + tile * kTileRows;
+        const size_t row_base = static_cast<size_t>(cur_b) * TH + tile * kTileRows;
         const size_t part_base =
             nsplit > 1 ? (static_cast<size_t>(slot + split) * TH + tile * kTileRows) : 0;
         const int rows_here = min(kTileRows, TH - tile * kTileRows);
