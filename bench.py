@@ -26,6 +26,7 @@ N > 1 runs under torch.distributed.run, one independent replica per GPU
 (the path needs no exchange between GPUs: weak scaling).
 """
 import argparse
+import copy
 import hashlib
 import json
 import os
@@ -360,8 +361,8 @@ class WorkloadRunner:
         else:
             self.m.up_project(self.W["w_uv"], self.out)
 
-    def plan(self):
-        self.m.plan(self.g.seq_lens)
+    def plan(self, g=None):
+        self.m.plan((self.g if g is None else g).seq_lens)
 
     def step(self):
         # One decode step as a caller makes it: the plan, then the whole run
@@ -370,8 +371,11 @@ class WorkloadRunner:
         self.plan()
         self.run_all()
 
-    def run_all(self):
-        g, W = self.g, self.W
+    def run_all(self, g=None, W=None):
+        # g, W: another device copy of the inputs and weights (the end-to-end
+        # run alternates two); by default the runner's own.
+        g = self.g if g is None else g
+        W = self.W if W is None else W
         if self.fp8:
             self.m.run_fp8w(g.q, g.cache, g.block_table, g.seq_lens, W["uk8"], W["uk_s"], W["uv8"],
                             W["uv_s"], g.scale, self.out, self.lse)
@@ -524,6 +528,7 @@ def main():
         dist.barrier()
     clocks.stop()
     r.check("in timed region")
+    want_out, want_lse = r.out.cpu(), r.lse.cpu()  # for the end-to-end check below
     elapsed = t_start.elapsed_time(t_end) / 1e3
 
     # Average duration of the dominant kernel (attention step): CUDA events on
@@ -534,35 +539,62 @@ def main():
     per_step = elapsed / args.steps
 
     # ---- end to end through the same C ABI with host buffers
-    host = [(getattr(inp_cpu, k).pin_memory(), getattr(g, k)) for k in
-            ("q", "cache", "block_table", "seq_lens")]
-    host += [(h.pin_memory(), dv) for h, dv in r.wts.values()]
+    # Every step copies all of its inputs from pinned host memory and reads
+    # its result back, in the form of a serving loop: two device copies of
+    # the inputs are used in turn, and step i + 1's inputs go up on a copy
+    # stream while step i computes (the copy into a set waits until the step
+    # that last read it has finished).
+    in_keys = ("q", "cache", "block_table", "seq_lens")
+    w_keys = list(r.wts)
+    host = [(getattr(inp_cpu, k).pin_memory(), k) for k in in_keys]
+    host_w = [(r.wts[k][0].pin_memory(), k) for k in w_keys]
+    g_alt = copy.copy(g)
+    for k in in_keys:
+        setattr(g_alt, k, torch.empty_like(getattr(g, k)))
+    dsets = [(g, r.W), (g_alt, {k: torch.empty_like(r.W[k]) for k in w_keys})]
     out_h = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
     lse_h = torch.empty(r.lse.shape, dtype=r.lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t, _ in host)
+    h2d = sum(t.numel() * t.element_size() for t, _ in host + host_w)
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    copy_stream = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event() for _ in dsets]
+    consumed = [torch.cuda.Event() for _ in dsets]
+    for ev in consumed:
+        ev.record(stream)
 
-    def e2e_step():
-        for t, dv in host:
-            dv.copy_(t, non_blocking=True)
-        r.plan()
-        r.run_all()
+    def e2e_step(i):
+        gj, wj = dsets[i % 2]
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(consumed[i % 2])
+            for t, k in host:
+                getattr(gj, k).copy_(t, non_blocking=True)
+            for t, k in host_w:
+                wj[k].copy_(t, non_blocking=True)
+            copied[i % 2].record(copy_stream)
+        stream.wait_event(copied[i % 2])
+        r.plan(gj)
+        r.run_all(gj, wj)
+        consumed[i % 2].record(stream)
         out_h.copy_(r.out, non_blocking=True)
         lse_h.copy_(r.lse, non_blocking=True)
 
     n_e2e = max(3, min(args.e2e_steps, args.steps))
-    for _ in range(3):
-        e2e_step()
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
     e0.record(stream)
-    for _ in range(n_e2e):
-        e2e_step()
+    copy_stream.wait_stream(stream)  # no copy of the timed steps starts before e0
+    for i in range(n_e2e):
+        e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     r.check("in the end-to-end run")
+    # The same inputs through either device set give the same bits.
+    if not (torch.equal(out_h, want_out) and torch.equal(lse_h, want_lse)):
+        raise SystemExit("end-to-end run: results read back differ from the timed steps'")
     e2e_s = e0.elapsed_time(e1) / 1e3 / n_e2e
     e2e_s = max_over_ranks(e2e_s, dist, dev)
 
@@ -645,7 +677,6 @@ def main():
         import oracle
         inp_or = inp_cpu
         if fp8:  # the oracle decompresses the FP8 weights, then decodes
-            import copy
             inp_or = copy.copy(inp_cpu)
             inp_or.w_uk = oracle.dequant_fp8_weight(wts_host["uk8"], wts_host["uk_s"])
             inp_or.w_uv = oracle.dequant_fp8_weight(wts_host["uv8"], wts_host["uv_s"])
