@@ -9,7 +9,9 @@ token per sequence, read once per step) summed over all ranks.  Also reports
 TFLOP/s (2176 FLOP per query row and key + the two bmms) and decode tokens/s,
 the roofline of the dominant kernel (the attention step) against the measured
 HBM copy bandwidth, an end-to-end figure through the same C ABI with host
-buffers, and the fp64 CPU oracle timed on a bounded sample.
+buffers (every step copies all of its inputs up from pinned host memory and
+reads its result back; the next step's copy overlaps this step's compute),
+and the fp64 CPU oracle timed on a bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
                   [--weights bf16|fp8] [--no-per-config]
